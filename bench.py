@@ -1,0 +1,430 @@
+"""Benchmark of the LatentMoE layer forward (one JSON line on rank 0).
+
+Default workload: the MAI-Base-1-shaped layer (T=16384 tokens, hidden 6656,
+latent 3072, 512 experts, top-8, SwiGLU FFN 10240, bf16, ~97 GB of expert
+weights resident). A step is one full forward through the C ABI. Inputs are
+larger than L2 (every step streams all touched expert weights from HBM).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, rank 0 only
+
+Multi-GPU runs are independent replicas (one process per GPU, weak scaling);
+the only collectives are the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LatentMoE bf16 fwd tokens/s at MAI-Base-1 shape; % of tensor-core roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DOMINANT = "expert_gate_up"
+GEMM_SRC = os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", "gemm.cuh")
+
+
+# ---------------------------------------------------------------- arithmetic
+
+def layer_flops_per_token(c) -> int:
+    """Router, latent down, k expert SwiGLU FFNs, latent up, shared expert."""
+    return 2 * c.d * c.E + 2 * c.d * c.l + 6 * c.k * c.l * c.F + 2 * c.l * c.d + 6 * c.d * c.Fs
+
+
+def layer_bytes(c, touched_experts: int) -> int:
+    """Algorithmic bytes: weights read once (experts that got tokens only),
+    x read once, y written once; intermediates excluded as avoidable."""
+    w = touched_experts * 3 * c.l * c.F * 2 + (c.E * c.d + 2 * c.l * c.d + 3 * c.d * c.Fs) * 2
+    return w + c.T * c.d * 2 * 2
+
+
+def gate_up_work(c, touched_experts: int):
+    """Per launch of the grouped gate+up GEMM: FLOPs and algorithmic bytes
+    (gate and up weights of touched experts, z rows read, h rows written)."""
+    S = c.T * c.k
+    flops = 2 * S * c.l * 2 * c.F
+    nbytes = touched_experts * 2 * c.F * c.l * 2 + S * c.l * 2 + S * c.F * 2
+    return flops, nbytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload}.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_tr):
+        return None
+    cur = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
+    return float(m_tr.group(1)) if m_sha.group(1) == cur else None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(1.0)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.count(",") >= 7]
+        os.unlink(self.file.name)
+        samples = []
+        for r in rows:
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                samples.append((ts, float(r[1]), float(r[2]), r[4:8]))
+            except Exception:
+                continue
+        inside = [s for s in samples if t0 - 1.0 <= s[0] <= t1 + 1.0] or samples
+        if not inside:
+            return None
+        mhz = sorted(s[1] for s in inside)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- oracle legs
+
+def oracle_tokens_per_s(cfg, x_rows, logits_rows, fetch, repeats=1):
+    """Time the float64 oracle on given token rows; returns (tokens/s, s)."""
+    from oracle import latentmoe_ref as ref
+    import numpy as np
+    W = ref.OracleWeights(fetch["w_r"], fetch["w_dn"], fetch["w_up"], fetch["expert"],
+                          b_r=fetch["b_r"], w_gs=fetch["w_gs"], w_us=fetch["w_us"],
+                          w_ds=fetch["w_ds"])
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        ref.forward(np.asarray(x_rows, dtype=np.float64), W, cfg.k, logits=logits_rows)
+    dt = time.perf_counter() - t0
+    return x_rows.shape[0] * repeats / dt, dt
+
+
+def host_weights(cfg, w, experts):
+    """bf16 weights as host float32 arrays (exact), with the experts needed."""
+    import numpy as np
+
+    def h(t):
+        return None if t is None else t.detach().float().cpu().numpy()
+    ex = {}
+    for e in experts:
+        if w.get("w_g") is not None:
+            ex[e] = (h(w["w_g"][e]), h(w["w_u"][e]), h(w["w_d"][e]))
+        else:
+            from mixture_experts_layer_router_gb300 import synth
+            dev = "cuda" if _cuda_ok() else "cpu"
+            ex[e] = tuple(h(t) for t in synth.make_expert(cfg, e, 0, dev))
+
+    def expert(e):
+        return tuple(a.astype(np.float64) for a in ex[e])
+    return {"w_r": h(w["w_r"]), "b_r": h(w["b_r"]), "w_dn": h(w["w_dn"]), "w_up": h(w["w_up"]),
+            "w_gs": h(w["w_gs"]), "w_us": h(w["w_us"]), "w_ds": h(w["w_ds"]), "expert": expert}
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, cfg, rank, world):
+    """The oracle on the host cores: each step is a bounded token sample."""
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+    from mixture_experts_layer_router_gb300 import synth
+    from oracle import latentmoe_ref as ref
+    dev = "cuda" if _cuda_ok() else "cpu"
+    n_steps = args.warmup + args.steps
+    per_step = args.ref_tokens
+    toks = synth.sample_tokens(cfg.T, n_steps * per_step, seed=1).numpy()
+    w = synth.make_weights(cfg, 0, dev, experts=False)
+    x = synth.make_x(cfg, 0, dev)
+    xs = x[torch.from_numpy(toks).to(dev)].float().cpu().numpy().astype(np.float64)
+    L = ref.router_logits(xs, w["w_r"].float().cpu().numpy().astype(np.float64),
+                          None if w["b_r"] is None else w["b_r"].cpu().numpy().astype(np.float64))
+    need = sorted(set(ref.top_k_stable(L, cfg.k).ravel().tolist()))
+    fetch = host_weights(cfg, w, need)
+    del w, x
+    times = []
+    for i in range(n_steps):
+        rows = slice(i * per_step, (i + 1) * per_step)
+        _, dt = oracle_tokens_per_s(cfg, xs[rows], None, fetch)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = args.steps * per_step / total
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} seeded token(s) of the {cfg.name} workload per "
+                                   "step, float64 NumPy oracle with its expert weights upcast "
+                                   "from host bf16 inside the timed work"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def workload_config(cfg):
+    return {"workload": f"{cfg.name} LatentMoE layer forward: T={cfg.T} d={cfg.d} l={cfg.l} "
+                        f"E={cfg.E} top-{cfg.k} F={cfg.F}" + (f" shared F={cfg.Fs}" if cfg.Fs else ""),
+            "T": cfg.T, "d": cfg.d, "l": cfg.l, "E": cfg.E, "k": cfg.k, "F": cfg.F, "Fs": cfg.Fs,
+            "l2": "inputs larger than L2 (all touched expert weights stream from HBM every step)",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, cfg, rank, world, dist):
+    import numpy as np
+    import torch
+    from mixture_experts_layer_router_gb300 import build, capi, synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(capi.LIB_PATH):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    capi.load()
+    w = synth.make_weights(cfg, 0, "cuda")
+    x = synth.make_x(cfg, 0, "cuda")
+    layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
+                           router_bias=w["b_r"] is not None)
+    layer.load_weights(w)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    assert layer.status() == 0, "device status set during warm-up"
+    r = layer.get_routing(cfg.T, "cuda")
+    counts = r["counts"].cpu().numpy()
+    touched = int((counts > 0).sum())
+    layer.set_profiling(args.steps)
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    launches0 = layer.launch_count()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(x, y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    launches = layer.launch_count() - launches0
+    clk = clocks.stop(wall0, wall1) if rank == 0 else None
+    stage_ms = {}
+    for s in range(args.steps):
+        for name, v in layer.stage_times(s).items():
+            stage_ms[name] = stage_ms.get(name, 0.0) + v / args.steps
+    status = layer.status()
+    layer.set_profiling(0)
+
+    if dist is not None:
+        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    # end to end through the host-buffer entry point: pinned x in, y out
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        yh = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+        layer.forward_host(xh, yh)
+        n_e2e = max(3, min(args.steps, 20))
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            layer.forward_host(xh, yh)
+        dt = time.perf_counter() - t0
+        if dist is not None:
+            tt = torch.tensor([dt], dtype=torch.float64, device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dt = float(tt.item())
+        e2e = {"value": world * cfg.T * n_e2e / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
+               "steps": n_e2e}
+
+    # CPU baseline: the oracle on a bounded token sample, rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import latentmoe_ref as ref  # noqa: F401
+        n = args.cpu_tokens
+        toks = synth.sample_tokens(cfg.T, n, seed=1)
+        tsel = toks.cuda()
+        L = r["logits"][tsel].double().cpu().numpy()
+        need = sorted(set(r["idx"][tsel].cpu().numpy().ravel().tolist()))
+        fetch = host_weights(cfg, w, need)
+        xs = x[tsel].float().cpu().numpy().astype(np.float64)
+        tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"{n} seeded tokens of the {cfg.name} workload ({dt:.1f} s), float64 "
+                         "NumPy oracle routed from the GPU logits, expert weights upcast from "
+                         "host bf16 inside the timed work"}
+
+    peaks, peak_src = load_peaks()
+    ms_step = ms_total / args.steps
+    value = world * cfg.T * args.steps / (ms_total / 1e3)
+    flops_tok = layer_flops_per_token(cfg)
+    lbytes = layer_bytes(cfg, touched)
+    tc_ms = cfg.T * flops_tok / (peaks["bf16_tflops_sustained"] * 1e12) * 1e3
+    hbm_ms = lbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    g_flops, g_bytes = gate_up_work(cfg, touched)
+    g_ms = stage_ms.get(DOMINANT, float("nan"))
+    g_tc = g_flops / (peaks["bf16_tflops_sustained"] * 1e12) * 1e3
+    g_hbm = g_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    if g_hbm >= g_tc:
+        roof = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": g_flops / (g_ms / 1e3) / 1e12,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(cfg.name)
+    roof.update({"kernel": DOMINANT, "ms_per_launch": g_ms, "algorithmic_bytes": g_bytes,
+                 "flops": g_flops, "tensor_tflops": g_flops / (g_ms / 1e3) / 1e12,
+                 "peak_source": f"{peak_src} ({'sustained bf16' if roof['bound'] == 'tensor' else 'HBM copy'})"})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
+        "config": workload_config(cfg),
+        "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
+        "tc_roofline_frac": tc_ms / ms_step,
+        "layer_roofline": {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms,
+                           "hbm_ms": hbm_ms, "roofline_ms": max(tc_ms, hbm_ms),
+                           "frac": max(tc_ms, hbm_ms) / ms_step, "touched_experts": touched,
+                           "peaks": {**peaks, "source": peak_src}},
+        "roofline": roof,
+        "stage_ms": stage_ms,
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "device_status": status,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mai-base-1")
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from mixture_experts_layer_router_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+        else:
+            tdist.init_process_group("gloo")
+        dist = tdist
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank, world)
+    else:
+        line = run_ours(args, cfg, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * latentmoe.h - C ABI of the LatentMoE layer forward for one GB300 (sm_103a).
+ *
+ * The layer (from "The Training and RL Infrastructure Behind MAI-Thinking-1",
+ * section "The model the systems run", and "MAI-Base-2: Microsoft's 2.8T base
+ * model, and whether its compute numbers add up", section "The model"):
+ *
+ *   L = x W_r^T (+ b)                       router on the full hidden state
+ *   p = softmax(L); idx = stable top-k of L  (ties: lower expert index first)
+ *   g[t,j] = p[t, idx[t,j]]                  (/ sum_j g if LATENTMOE_RENORM)
+ *   z = x W_dn^T                             shared down-projection to the latent
+ *   slots sorted by expert (counting sort, token order kept inside an expert)
+ *   H = (SiLU(z W_g^T) * (z W_u^T)) W_d^T    per-expert SwiGLU on the latent
+ *   c[t] = sum_j g[t,j] H[pos[t,j]]          gate-weighted combine, fp32, j order
+ *   y = c W_up^T (+ (SiLU(x W_gs^T) * (x W_us^T)) W_ds^T)   up-projection + shared
+ *
+ * Conventions for every entry point:
+ * - Return 0 (LATENTMOE_OK) on success, a negative LATENTMOE_ERR_* otherwise.
+ *   No C++ exception crosses the ABI and no kernel traps.
+ * - "device pointer" means memory the current CUDA device can address
+ *   (cudaMalloc or a PyTorch CUDA tensor's data_ptr()). The caller owns every
+ *   pointer it passes. Pointers must be 16-byte aligned.
+ * - Work is enqueued on the caller's stream and returns without waiting,
+ *   unless the entry says it synchronises. Launch errors are returned at
+ *   once; errors found by kernels set a device status word that
+ *   latentmoe_get_status reads.
+ * - A handle is not thread-safe; use it from one host thread and one stream
+ *   at a time. One GPU only: the handle belongs to the device that was
+ *   current at latentmoe_create.
+ * - Matrices are row-major in torch nn.Linear layout [out, in]; bf16 means
+ *   IEEE bfloat16 stored as 16-bit words.
+ */
+#ifndef LATENTMOE_H
+#define LATENTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct latentmoe* latentmoe_t;
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* latentmoe_stream_t;
+
+/* Layer dimensions. hidden d, latent l, ffn F and shared_ffn F_s must be
+ * multiples of 128 (F_s may be 0: no shared expert). 1 <= num_experts E <= 512.
+ * max_tokens bounds T for every forward and sizes the workspace. */
+typedef struct {
+  int64_t hidden;
+  int64_t latent;
+  int64_t num_experts;
+  int64_t ffn;
+  int64_t shared_ffn;
+  int64_t max_tokens;
+} latentmoe_dims;
+
+/* Device pointers to the weights, all bf16 except b_r (fp32).
+ *   w_r  [E, d]        router               b_r [E] (LATENTMOE_ROUTER_BIAS only)
+ *   w_dn [l, d]        latent down          w_up [d, l]   latent up
+ *   w_g, w_u [E, F, l] expert gate and up   w_d [E, l, F] expert down
+ *   w_gs, w_us [F_s, d], w_ds [d, F_s]      shared expert (F_s > 0 only)
+ * The stacked expert tensors are contiguous, expert-major. */
+typedef struct {
+  const void* w_r;
+  const float* b_r;
+  const void* w_dn;
+  const void* w_g;
+  const void* w_u;
+  const void* w_d;
+  const void* w_up;
+  const void* w_gs;
+  const void* w_us;
+  const void* w_ds;
+} latentmoe_weights;
+
+enum {
+  LATENTMOE_RENORM = 1u,      /* divide the k gates of a token by their sum */
+  LATENTMOE_ROUTER_BIAS = 2u, /* add b_r to the logits (selection and softmax) */
+  LATENTMOE_OUT_FP32 = 4u     /* forward output y is fp32 instead of bf16 */
+};
+
+enum {
+  LATENTMOE_OK = 0,
+  LATENTMOE_ERR_INVALID_ARG = -1,   /* NULL, T <= 0, T > max_tokens, k > E, k > 16 ... */
+  LATENTMOE_ERR_UNSUPPORTED = -2,   /* dims not multiples of 128, E > 512, misaligned */
+  LATENTMOE_ERR_NOT_LOADED = -3,    /* forward before latentmoe_load_weights */
+  LATENTMOE_ERR_CUDA = -4,          /* a CUDA call failed; see latentmoe_last_cuda_error */
+  LATENTMOE_ERR_TIMEOUT = -5,       /* a bounded device-side wait gave up */
+  LATENTMOE_ERR_DEVICE_STATUS = -6, /* a kernel flagged bad data (e.g. expert id out of range) */
+  LATENTMOE_ERR_OUT_OF_MEMORY = -7  /* workspace allocation failed */
+};
+
+/* Device status bits returned by latentmoe_get_status. */
+enum {
+  LATENTMOE_STATUS_TIMEOUT = 1u,    /* a pipeline wait in a GEMM kernel gave up */
+  LATENTMOE_STATUS_BAD_EXPERT = 2u  /* an expert id outside [0, E) reached the sort */
+};
+
+/* Create a handle on the current device: validates dims, top_k (1..16,
+ * <= E) and flags, and allocates the workspace for max_tokens tokens
+ * (intermediates z, h, o, c, routing metadata; about
+ * max_tokens*k*(2l+F)*2 bytes). Defined by the layer statement above.
+ * On error *out is left NULL and nothing stays allocated. */
+int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags,
+                     latentmoe_t* out);
+
+/* Bind the weights (device pointers, layouts in latentmoe_weights). The
+ * library does not copy them: they are used in place by every later forward,
+ * so the caller keeps them alive and unchanged until latentmoe_destroy or
+ * the next latentmoe_load_weights. Builds the TMA descriptors; enqueues no
+ * GPU work. Errors: INVALID_ARG (NULL pointer that the dims or flags need),
+ * UNSUPPORTED (pointer not 16-byte aligned). */
+int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w);
+
+/* The layer forward. x: device bf16 [T, d]; out: device [T, d], bf16 (fp32
+ * with LATENTMOE_OUT_FP32). 1 <= T <= max_tokens. Asynchronous on `stream`;
+ * no host synchronisation and no device-to-host copy happen inside.
+ * out must not overlap x or the weights. Bitwise deterministic for fixed
+ * inputs and device. */
+int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T,
+                      latentmoe_stream_t stream);
+
+/* The same forward with HOST buffers: copies x_host (bf16 [T, d]) to the
+ * device, runs latentmoe_forward, copies the result to out_host, and
+ * synchronises `stream` before returning. Page-locked host memory gives
+ * full copy speed; pageable memory works too. Staging buffers are allocated
+ * on the first call and kept by the handle. */
+int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host,
+                           int64_t T, latentmoe_stream_t stream);
+
+/* Free the workspace and the handle. NULL is accepted and ignored. */
+int latentmoe_destroy(latentmoe_t h);
+
+/* Routing from given logits (the router-replay hook and the integer parity
+ * test): from fp32 logits [T, E] (device) computes, on `stream`,
+ *   idx [T, k] int32, gates [T, k] fp32   (softmax over E, stable top-k)
+ *   counts [E], offsets [E+1], perm [T*k], pos [T, k]   int32 (counting sort)
+ * with the handle's k and LATENTMOE_RENORM flag. All outputs are device
+ * pointers; any of counts/offsets/perm/pos may be NULL to skip the copy. */
+int latentmoe_route_from_logits(latentmoe_t h, const float* logits, int64_t T,
+                                int32_t* idx, float* gates, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* pos,
+                                latentmoe_stream_t stream);
+
+/* Copy the routing state of the last forward on this handle into caller
+ * device buffers (each may be NULL): logits [T, E] fp32 (bias included),
+ * idx, gates, counts, offsets, perm, pos as in latentmoe_route_from_logits.
+ * Enqueued on `stream`; T is the last forward's token count. */
+int latentmoe_get_routing(latentmoe_t h, float* logits, int32_t* idx,
+                          float* gates, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* pos, latentmoe_stream_t stream);
+
+/* Synchronise the device, then read and clear the device status word
+ * (LATENTMOE_STATUS_* bits). Returns TIMEOUT or DEVICE_STATUS when bits
+ * were set, CUDA on a CUDA error, else OK. */
+int latentmoe_get_status(latentmoe_t h, uint32_t* device_status);
+
+/* Stage timing. latentmoe_set_profiling(h, n) with n > 0 makes each forward
+ * record CUDA events between its stages into one of n rotating slots
+ * (forward i uses slot i % n); n = 0 turns it off. latentmoe_get_stage_times
+ * synchronises on the slot's last event and writes up to `count` per-stage
+ * durations in milliseconds, in the order of latentmoe_stage_name. */
+int latentmoe_set_profiling(latentmoe_t h, int slots);
+int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count);
+int latentmoe_num_stages(void);
+const char* latentmoe_stage_name(int stage);
+
+/* Kernel launches issued by this handle since creation. */
+int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches);
+
+/* Last CUDA error code (cudaError_t value) seen by the handle, 0 if none. */
+int latentmoe_last_cuda_error(latentmoe_t h);
+
+/* Static description of a return code. */
+const char* latentmoe_strerror(int code);
+
+/* ---- Debug entry points: the tensor-core GEMM core on its own. ----------
+ * C = epilogue(A B^T) for bf16 A [M, K] and B [N', K] (device, row-major).
+ *   mode 0: C bf16 [M, N], B has N rows
+ *   mode 1: C fp32 [M, N], B has N rows
+ *   mode 2: C bf16 [M, N] = SiLU(A Bg^T) * (A Bu^T); B is [2, G*N, K]: the
+ *           gate rows of all groups, then the up rows of all groups (G = 1
+ *           for the dense entry, i.e. Bg = rows 0..N-1, Bu = rows N..2N-1)
+ * M >= 1, K and N multiples of 128 (mode 1: N >= 1). Grouped variant: rows
+ * of A and C are split by device int32 offsets [G+1] (offsets[0] = 0,
+ * non-decreasing, offsets[G] <= M, G <= 512); group g multiplies with rows
+ * [g*N, (g+1)*N) of B (of each half of B in mode 2).
+ * Asynchronous on `stream`; errors as above. */
+int latentmoe_debug_gemm(const void* A, const void* B, void* C, int64_t M,
+                         int64_t N, int64_t K, int mode,
+                         latentmoe_stream_t stream);
+int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C,
+                                 const int32_t* offsets, int64_t groups,
+                                 int64_t M, int64_t N, int64_t K, int mode,
+                                 latentmoe_stream_t stream);
+/* Device status word of the debug entry points (synchronises, then clears). */
+int latentmoe_debug_status(uint32_t* device_status);
+
+/* Exercise the bounded device wait: one thread waits on an mbarrier that
+ * nothing completes, gives up after limit_ns (<= 1 s) and sets
+ * LATENTMOE_STATUS_TIMEOUT. Synchronises; returns LATENTMOE_ERR_TIMEOUT and
+ * the status bits when the wait gave up as designed. */
+int latentmoe_debug_wait_timeout(uint64_t limit_ns, uint32_t* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LATENTMOE_H */

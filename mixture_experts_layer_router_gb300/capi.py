@@ -1,0 +1,253 @@
+"""ctypes binding of liblatentmoe.so (include/latentmoe.h), same names.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels. PyTorch provides device memory (``tensor.data_ptr()``) and
+streams (``torch.cuda.current_stream().cuda_stream``). There is no fallback:
+``load()`` raises if the library is missing or cannot be loaded.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "liblatentmoe.so")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_NOT_LOADED = -3
+ERR_CUDA = -4
+ERR_TIMEOUT = -5
+ERR_DEVICE_STATUS = -6
+ERR_OUT_OF_MEMORY = -7
+
+RENORM = 1
+ROUTER_BIAS = 2
+OUT_FP32 = 4
+
+STATUS_TIMEOUT = 1
+STATUS_BAD_EXPERT = 2
+
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class latentmoe_dims(ctypes.Structure):
+    _fields_ = [("hidden", _i64), ("latent", _i64), ("num_experts", _i64),
+                ("ffn", _i64), ("shared_ffn", _i64), ("max_tokens", _i64)]
+
+
+class latentmoe_weights(ctypes.Structure):
+    _fields_ = [(n, _c_void_p) for n in
+                ("w_r", "b_r", "w_dn", "w_g", "w_u", "w_d", "w_up", "w_gs", "w_us", "w_ds")]
+
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "latentmoe_create": (ctypes.c_int, [ctypes.POINTER(latentmoe_dims), ctypes.c_int,
+                                        ctypes.c_uint32, ctypes.POINTER(_c_void_p)]),
+    "latentmoe_load_weights": (ctypes.c_int, [_c_void_p, ctypes.POINTER(latentmoe_weights)]),
+    "latentmoe_forward": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
+    "latentmoe_forward_host": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
+    "latentmoe_destroy": (ctypes.c_int, [_c_void_p]),
+    "latentmoe_route_from_logits": (ctypes.c_int, [_c_void_p, _c_void_p, _i64] + [_c_void_p] * 7),
+    "latentmoe_get_routing": (ctypes.c_int, [_c_void_p] + [_c_void_p] * 7 + [_c_void_p]),
+    "latentmoe_get_status": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "latentmoe_set_profiling": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
+    "latentmoe_get_stage_times": (ctypes.c_int, [_c_void_p, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_float), ctypes.c_int]),
+    "latentmoe_num_stages": (ctypes.c_int, []),
+    "latentmoe_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "latentmoe_get_launch_count": (ctypes.c_int, [_c_void_p, ctypes.POINTER(_i64)]),
+    "latentmoe_last_cuda_error": (ctypes.c_int, [_c_void_p]),
+    "latentmoe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "latentmoe_debug_gemm": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
+                                            ctypes.c_int, _c_void_p]),
+    "latentmoe_debug_grouped_gemm": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                                    _i64, _i64, _i64, _i64, ctypes.c_int,
+                                                    _c_void_p]),
+    "latentmoe_debug_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "latentmoe_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64,
+                                                    ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once) and declare every entry point."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first "
+                           "(python -m mixture_experts_layer_router_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class LatentMoEError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = load().latentmoe_strerror(code).decode()
+        super().__init__(f"{what}: {msg} ({code})")
+
+
+def check(code: int, what: str) -> None:
+    if code != OK:
+        raise LatentMoEError(code, what)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class LatentMoE:
+    """A handle plus the torch tensors it borrows.
+
+    ``weights`` is a dict as made by ``synth.make_weights`` (device bf16
+    tensors, ``b_r`` fp32 or None). The tensors are kept referenced here
+    because the library uses them in place.
+    """
+
+    def __init__(self, d: int, l: int, E: int, k: int, F: int, Fs: int = 0,
+                 max_tokens: int = 1, renorm: bool = False, router_bias: bool = False,
+                 out_fp32: bool = False):
+        lib = load()
+        self.dims = latentmoe_dims(d, l, E, F, Fs, max_tokens)
+        self.k = k
+        self.flags = (RENORM if renorm else 0) | (ROUTER_BIAS if router_bias else 0) | \
+            (OUT_FP32 if out_fp32 else 0)
+        h = _c_void_p()
+        check(lib.latentmoe_create(ctypes.byref(self.dims), k, self.flags, ctypes.byref(h)),
+              "latentmoe_create")
+        self.handle = h
+        self._weights: Dict[str, object] = {}
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            load().latentmoe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load_weights(self, w: Dict[str, object]) -> None:
+        lw = latentmoe_weights(*(_ptr(w.get(n)) for n in
+                                 ("w_r", "b_r", "w_dn", "w_g", "w_u", "w_d", "w_up",
+                                  "w_gs", "w_us", "w_ds")))
+        check(load().latentmoe_load_weights(self.handle, ctypes.byref(lw)),
+              "latentmoe_load_weights")
+        self._weights = dict(w)
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if out is None:
+            dt = torch.float32 if self.flags & OUT_FP32 else torch.bfloat16
+            out = torch.empty((T, self.dims.hidden), dtype=dt, device=x.device)
+        check(load().latentmoe_forward(self.handle, x.data_ptr(), out.data_ptr(), T,
+                                       _stream(stream)), "latentmoe_forward")
+        return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        check(load().latentmoe_forward_host(self.handle, x_host.data_ptr(), out_host.data_ptr(),
+                                            x_host.shape[0], _stream(stream)),
+              "latentmoe_forward_host")
+        return out_host
+
+    def route_from_logits(self, logits, stream=None):
+        import torch
+        T, E = logits.shape
+        dev = logits.device
+        k = self.k
+        out = {
+            "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+            "gates": torch.empty((T, k), dtype=torch.float32, device=dev),
+            "counts": torch.empty((E,), dtype=torch.int32, device=dev),
+            "offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+            "perm": torch.empty((T * k,), dtype=torch.int32, device=dev),
+            "pos": torch.empty((T, k), dtype=torch.int32, device=dev),
+        }
+        check(load().latentmoe_route_from_logits(
+            self.handle, logits.data_ptr(), T, out["idx"].data_ptr(), out["gates"].data_ptr(),
+            out["counts"].data_ptr(), out["offsets"].data_ptr(), out["perm"].data_ptr(),
+            out["pos"].data_ptr(), _stream(stream)), "latentmoe_route_from_logits")
+        return out
+
+    def get_routing(self, T: int, device, stream=None):
+        import torch
+        E, k = self.dims.num_experts, self.k
+        out = {
+            "logits": torch.empty((T, E), dtype=torch.float32, device=device),
+            "idx": torch.empty((T, k), dtype=torch.int32, device=device),
+            "gates": torch.empty((T, k), dtype=torch.float32, device=device),
+            "counts": torch.empty((E,), dtype=torch.int32, device=device),
+            "offsets": torch.empty((E + 1,), dtype=torch.int32, device=device),
+            "perm": torch.empty((T * k,), dtype=torch.int32, device=device),
+            "pos": torch.empty((T, k), dtype=torch.int32, device=device),
+        }
+        check(load().latentmoe_get_routing(
+            self.handle, *(out[n].data_ptr() for n in
+                           ("logits", "idx", "gates", "counts", "offsets", "perm", "pos")),
+            _stream(stream)), "latentmoe_get_routing")
+        return out
+
+    def status(self) -> int:
+        v = ctypes.c_uint32(0)
+        load().latentmoe_get_status(self.handle, ctypes.byref(v))
+        return v.value
+
+    def set_profiling(self, slots: int) -> None:
+        check(load().latentmoe_set_profiling(self.handle, slots), "latentmoe_set_profiling")
+
+    def stage_times(self, slot: int):
+        n = load().latentmoe_num_stages()
+        buf = (ctypes.c_float * n)()
+        check(load().latentmoe_get_stage_times(self.handle, slot, buf, n),
+              "latentmoe_get_stage_times")
+        return {stage_name(i): buf[i] for i in range(n)}
+
+    def launch_count(self) -> int:
+        v = _i64(0)
+        check(load().latentmoe_get_launch_count(self.handle, ctypes.byref(v)),
+              "latentmoe_get_launch_count")
+        return v.value
+
+
+def stage_name(i: int) -> str:
+    return load().latentmoe_stage_name(i).decode()
+
+
+def debug_gemm(A, B, C, M: int, N: int, K: int, mode: int, stream=None) -> int:
+    return load().latentmoe_debug_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, mode,
+                                       _stream(stream))
+
+
+def debug_grouped_gemm(A, B, C, offsets, groups: int, M: int, N: int, K: int, mode: int,
+                       stream=None) -> int:
+    return load().latentmoe_debug_grouped_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                               offsets.data_ptr(), groups, M, N, K, mode,
+                                               _stream(stream))
+
+
+def debug_status() -> int:
+    v = ctypes.c_uint32(0)
+    load().latentmoe_debug_status(ctypes.byref(v))
+    return v.value

@@ -1,0 +1,721 @@
+// C ABI of the LatentMoE layer forward (declared in include/latentmoe.h).
+//
+// Host code only: validation, workspace, TMA descriptors and the launch
+// sequence. All arithmetic of the layer runs in the kernels of this library.
+//
+// Launch sequence of latentmoe_forward, all on the caller's stream with no
+// host synchronisation (token counts per expert stay on the device, as in
+// "Frontier Pre-training at Microsoft AI", section "Reducing per-expert
+// overhead"):
+//   0 router_gemm     logits = x W_r^T (+ b)                 tcgen05, fp32 out
+//   1 route_topk      softmax + stable top-k                 warp per token
+//   2 sort            counts, offsets, perm, pos             3 small kernels
+//   3 down_proj       z = x W_dn^T, written to the k slots   tcgen05, scatter
+//   4 expert_gate_up  h = SiLU(z W_g^T) * (z W_u^T)          tcgen05, grouped
+//   5 expert_down     o = h W_d^T                            tcgen05, grouped
+//   6 combine         c[t] = sum_j g[t,j] o[pos[t,j]]        gather, fp32
+//   7 shared_gate_up  s = SiLU(x W_gs^T) * (x W_us^T)        tcgen05 (F_s > 0)
+//   8 up_proj         y = c W_up^T (+ s W_ds^T)              tcgen05, dual-K
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "kernels.h"
+#include "latentmoe.h"
+
+using lmoe::GemmArgs;
+using lmoe::GemmMaps;
+
+namespace {
+
+constexpr int kNumStages = 9;
+const char* const kStageNames[kNumStages] = {
+    "router_gemm", "route_topk", "sort",   "down_proj", "expert_gate_up",
+    "expert_down", "combine",    "shared_gate_up", "up_proj"};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row stride `ld` elements) read in boxes of
+// 64 columns x box_rows rows with 128-byte swizzle; out-of-range reads are 0.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+}  // namespace
+
+struct latentmoe {
+  latentmoe_dims dims;
+  int k = 0;
+  uint32_t flags = 0;
+  int device = 0;
+  int sms = 1;
+  bool loaded = false;
+  latentmoe_weights w;
+  GemmMaps m_router, m_down, m_gate_up, m_expert_down, m_shared, m_up;
+  // workspace
+  void* ws = nullptr;
+  float* logits = nullptr;
+  int* idx = nullptr;
+  float* gates = nullptr;
+  int* cnt = nullptr;
+  int* cbase = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* perm = nullptr;
+  int* pos = nullptr;
+  __nv_bfloat16* zp = nullptr;
+  __nv_bfloat16* hb = nullptr;
+  __nv_bfloat16* ob = nullptr;
+  __nv_bfloat16* cb = nullptr;
+  __nv_bfloat16* sh = nullptr;
+  unsigned* status = nullptr;
+  int64_t last_T = 0;
+  // host-buffer forward staging
+  void* x_stage = nullptr;
+  void* y_stage = nullptr;
+  // profiling
+  std::vector<cudaEvent_t> events;
+  int prof_slots = 0;
+  int64_t forwards = 0;
+  int64_t launches = 0;
+  int last_cuda = 0;
+};
+
+namespace {
+
+int fail_cuda(latentmoe* h, cudaError_t e) {
+  if (h != nullptr) h->last_cuda = static_cast<int>(e);
+  return e == cudaErrorMemoryAllocation ? LATENTMOE_ERR_OUT_OF_MEMORY : LATENTMOE_ERR_CUDA;
+}
+
+#define LMOE_CK(h, call)                          \
+  do {                                            \
+    const cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return fail_cuda(h, e_); \
+  } while (0)
+
+GemmArgs base_args(const latentmoe* h) {
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.group_m = 16;
+  a.status = h->status;
+  return a;
+}
+
+int dense_grid(const latentmoe* h, int M, int n_tiles) {
+  const long long tiles = static_cast<long long>((M + lmoe::kBM - 1) / lmoe::kBM) * n_tiles;
+  return static_cast<int>(tiles < h->sms ? tiles : h->sms);
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+void record(latentmoe* h, int slot_base, int i, cudaStream_t s) {
+  if (h->prof_slots > 0) cudaEventRecord(h->events[slot_base + i], s);
+}
+
+// Routing half shared by forward and route_from_logits: logits -> idx,
+// gates -> counts, offsets, perm, pos (workspace buffers).
+int run_routing(latentmoe* h, const float* logits, int T, cudaStream_t s, int slot_base) {
+  const int E = static_cast<int>(h->dims.num_experts);
+  const int S = T * h->k;
+  LMOE_CK(h, lmoe::launch_route_topk(logits, T, E, h->k, (h->flags & LATENTMOE_RENORM) ? 1 : 0,
+                                     h->idx, h->gates, s));
+  h->launches += 1;
+  record(h, slot_base, 2, s);
+  LMOE_CK(h, lmoe::launch_sort(h->idx, S, h->k, E, h->cnt, h->cbase, h->counts, h->offsets,
+                               h->perm, h->pos, h->status, s));
+  h->launches += lmoe::kSortLaunches;
+  record(h, slot_base, 3, s);
+  return LATENTMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int latentmoe_num_stages(void) { return kNumStages; }
+
+const char* latentmoe_stage_name(int stage) {
+  return (stage >= 0 && stage < kNumStages) ? kStageNames[stage] : nullptr;
+}
+
+const char* latentmoe_strerror(int code) {
+  switch (code) {
+    case LATENTMOE_OK: return "ok";
+    case LATENTMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LATENTMOE_ERR_UNSUPPORTED: return "unsupported dimensions, flags or alignment";
+    case LATENTMOE_ERR_NOT_LOADED: return "weights not loaded";
+    case LATENTMOE_ERR_CUDA: return "CUDA error";
+    case LATENTMOE_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case LATENTMOE_ERR_DEVICE_STATUS: return "a kernel flagged invalid data";
+    case LATENTMOE_ERR_OUT_OF_MEMORY: return "out of device memory";
+    default: return "unknown error";
+  }
+}
+
+int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, latentmoe_t* out) {
+  if (out == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (dims == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  const latentmoe_dims d = *dims;
+  if (flags & ~static_cast<uint32_t>(LATENTMOE_RENORM | LATENTMOE_ROUTER_BIAS |
+                                     LATENTMOE_OUT_FP32))
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (d.num_experts < 1 || d.max_tokens < 1 || d.hidden < 1 || d.latent < 1 || d.ffn < 1 ||
+      d.shared_ffn < 0)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > 16 || top_k > d.num_experts) return LATENTMOE_ERR_INVALID_ARG;
+  if (d.num_experts > lmoe::kMaxGroups) return LATENTMOE_ERR_UNSUPPORTED;
+  if (d.hidden % 128 || d.latent % 128 || d.ffn % 128 || d.shared_ffn % 128)
+    return LATENTMOE_ERR_UNSUPPORTED;
+  const long long S = d.max_tokens * top_k;
+  if (S > (1ll << 30) || d.hidden > (1 << 20) || d.latent > (1 << 20) || d.ffn > (1 << 20) ||
+      d.shared_ffn > (1 << 20))
+    return LATENTMOE_ERR_UNSUPPORTED;
+  // rows of the stacked expert weights are addressed with int32 TMA coordinates
+  if (d.num_experts * d.ffn >= (1ll << 31) || d.num_experts * d.latent >= (1ll << 31))
+    return LATENTMOE_ERR_UNSUPPORTED;
+
+  latentmoe* h = new (std::nothrow) latentmoe();
+  if (h == nullptr) return LATENTMOE_ERR_OUT_OF_MEMORY;
+  h->dims = d;
+  h->k = top_k;
+  h->flags = flags;
+  memset(&h->w, 0, sizeof(h->w));
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return LATENTMOE_ERR_CUDA;
+  }
+  h->sms = num_sms();
+
+  const long long T = d.max_tokens, E = d.num_experts, l = d.latent, F = d.ffn;
+  const long long Fs = d.shared_ffn;
+  const long long nb_ints = lmoe::sort_scratch_ints(S, E);
+  const size_t al = 1024;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, al);
+    return o;
+  };
+  const size_t o_logits = take(T * E * 4);
+  const size_t o_idx = take(S * 4), o_gates = take(S * 4), o_perm = take(S * 4),
+               o_pos = take(S * 4);
+  const size_t o_cnt = take(nb_ints * 4), o_cbase = take(nb_ints * 4);
+  const size_t o_counts = take(E * 4), o_offsets = take((E + 1) * 4);
+  const size_t o_zp = take(S * l * 2), o_h = take(S * F * 2), o_o = take(S * l * 2);
+  const size_t o_c = take(T * l * 2), o_sh = take(Fs > 0 ? T * Fs * 2 : 16);
+  const size_t o_status = take(16);
+  e = cudaMalloc(&h->ws, off);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return e == cudaErrorMemoryAllocation ? LATENTMOE_ERR_OUT_OF_MEMORY : LATENTMOE_ERR_CUDA;
+  }
+  char* base = static_cast<char*>(h->ws);
+  h->logits = reinterpret_cast<float*>(base + o_logits);
+  h->idx = reinterpret_cast<int*>(base + o_idx);
+  h->gates = reinterpret_cast<float*>(base + o_gates);
+  h->perm = reinterpret_cast<int*>(base + o_perm);
+  h->pos = reinterpret_cast<int*>(base + o_pos);
+  h->cnt = reinterpret_cast<int*>(base + o_cnt);
+  h->cbase = reinterpret_cast<int*>(base + o_cbase);
+  h->counts = reinterpret_cast<int*>(base + o_counts);
+  h->offsets = reinterpret_cast<int*>(base + o_offsets);
+  h->zp = reinterpret_cast<__nv_bfloat16*>(base + o_zp);
+  h->hb = reinterpret_cast<__nv_bfloat16*>(base + o_h);
+  h->ob = reinterpret_cast<__nv_bfloat16*>(base + o_o);
+  h->cb = reinterpret_cast<__nv_bfloat16*>(base + o_c);
+  h->sh = reinterpret_cast<__nv_bfloat16*>(base + o_sh);
+  h->status = reinterpret_cast<unsigned*>(base + o_status);
+  e = cudaMemset(h->status, 0, 16);
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return LATENTMOE_ERR_CUDA;
+  }
+  *out = h;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_destroy(latentmoe_t h) {
+  if (h == nullptr) return LATENTMOE_OK;
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  if (h->x_stage) cudaFree(h->x_stage);
+  if (h->y_stage) cudaFree(h->y_stage);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
+  if (h == nullptr || w == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  const latentmoe_dims& d = h->dims;
+  const bool shared = d.shared_ffn > 0;
+  const bool bias = (h->flags & LATENTMOE_ROUTER_BIAS) != 0;
+  if (!w->w_r || !w->w_dn || !w->w_g || !w->w_u || !w->w_d || !w->w_up)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (bias && !w->b_r) return LATENTMOE_ERR_INVALID_ARG;
+  if (shared && (!w->w_gs || !w->w_us || !w->w_ds)) return LATENTMOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->w_r, w->w_dn, w->w_g, w->w_u, w->w_d, w->w_up};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LATENTMOE_ERR_UNSUPPORTED;
+  if (shared && (!aligned16(w->w_gs) || !aligned16(w->w_us) || !aligned16(w->w_ds)))
+    return LATENTMOE_ERR_UNSUPPORTED;
+  if (bias && (reinterpret_cast<uintptr_t>(w->b_r) & 3u)) return LATENTMOE_ERR_UNSUPPORTED;
+  LMOE_CK(h, cudaSetDevice(h->device));
+
+  const uint64_t E = d.num_experts, dd = d.hidden, l = d.latent, F = d.ffn, Fs = d.shared_ffn;
+  bool ok = true;
+  ok &= make_map(&h->m_router.b, w->w_r, E, dd, dd, 256);
+  ok &= make_map(&h->m_down.b, w->w_dn, l, dd, dd, 256);
+  ok &= make_map(&h->m_gate_up.b, w->w_g, E * F, l, l, 128);
+  ok &= make_map(&h->m_gate_up.bu, w->w_u, E * F, l, l, 128);
+  ok &= make_map(&h->m_expert_down.b, w->w_d, E * l, F, F, 256);
+  ok &= make_map(&h->m_up.b, w->w_up, dd, l, l, 256);
+  if (shared) {
+    ok &= make_map(&h->m_shared.b, w->w_gs, Fs, dd, dd, 128);
+    ok &= make_map(&h->m_shared.bu, w->w_us, Fs, dd, dd, 128);
+    ok &= make_map(&h->m_up.b2, w->w_ds, dd, Fs, Fs, 256);
+  }
+  if (!ok) return LATENTMOE_ERR_CUDA;
+  // unused map slots still travel as kernel parameters: give them a valid copy
+  h->m_router.bu = h->m_router.a2 = h->m_router.b2 = h->m_router.b;
+  h->m_down.bu = h->m_down.a2 = h->m_down.b2 = h->m_down.b;
+  h->m_gate_up.a2 = h->m_gate_up.b2 = h->m_gate_up.b;
+  h->m_expert_down.bu = h->m_expert_down.a2 = h->m_expert_down.b2 = h->m_expert_down.b;
+  if (shared) {
+    h->m_shared.a2 = h->m_shared.b2 = h->m_shared.b;
+  } else {
+    h->m_up.b2 = h->m_up.b;
+  }
+  h->m_up.bu = h->m_up.b;
+  h->w = *w;
+  h->loaded = true;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latentmoe_stream_t st) {
+  if (h == nullptr || x == nullptr || out == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
+  if (!aligned16(x) || !aligned16(out)) return LATENTMOE_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const latentmoe_dims& d = h->dims;
+  const int E = static_cast<int>(d.num_experts), k = h->k;
+  const int dd = static_cast<int>(d.hidden), l = static_cast<int>(d.latent);
+  const int F = static_cast<int>(d.ffn), Fs = static_cast<int>(d.shared_ffn);
+  const int Ti = static_cast<int>(T), S = Ti * k;
+  const bool out32 = (h->flags & LATENTMOE_OUT_FP32) != 0;
+
+  // activation maps for this call
+  CUtensorMap mx, mzp, mh, mc, msh;
+  bool ok = make_map(&mx, x, T, dd, dd, 128);
+  ok &= make_map(&mzp, h->zp, S, l, l, 128);
+  ok &= make_map(&mh, h->hb, S, F, F, 128);
+  ok &= make_map(&mc, h->cb, T, l, l, 128);
+  if (Fs > 0) ok &= make_map(&msh, h->sh, T, Fs, Fs, 128);
+  if (!ok) return LATENTMOE_ERR_CUDA;
+
+  const int slot_base = h->prof_slots > 0
+                            ? static_cast<int>(h->forwards % h->prof_slots) * (kNumStages + 1)
+                            : 0;
+  h->forwards += 1;
+  record(h, slot_base, 0, s);
+
+  // 0: router logits (fp32, + bias)
+  {
+    GemmMaps m = h->m_router;
+    m.a = mx;
+    GemmArgs a = base_args(h);
+    a.M = Ti;
+    a.N = E;
+    a.n_tiles = ceil_div(E, lmoe::kBN);
+    a.kb1 = dd / lmoe::kBK;
+    a.out = h->logits;
+    a.ldo = E;
+    a.bias = (h->flags & LATENTMOE_ROUTER_BIAS) ? h->w.b_r : nullptr;
+    LMOE_CK(h, lmoe::launch_gemm_f32(m, a, dense_grid(h, Ti, a.n_tiles), false, s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 1, s);
+  // 1-2: softmax + top-k, counting sort
+  {
+    const int r = run_routing(h, h->logits, Ti, s, slot_base);
+    if (r != LATENTMOE_OK) return r;
+  }
+  // 3: latent down-projection scattered to the expert-sorted slots
+  {
+    GemmMaps m = h->m_down;
+    m.a = mx;
+    GemmArgs a = base_args(h);
+    a.M = Ti;
+    a.N = l;
+    a.n_tiles = ceil_div(l, lmoe::kBN);
+    a.kb1 = dd / lmoe::kBK;
+    a.out = h->zp;
+    a.ldo = l;
+    a.pos = h->pos;
+    a.topk = k;
+    LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 4, s);
+  // 4: grouped gate+up with SwiGLU
+  {
+    GemmMaps m = h->m_gate_up;
+    m.a = mzp;
+    GemmArgs a = base_args(h);
+    a.grouped = 1;
+    a.num_groups = E;
+    a.seg_offsets = h->offsets;
+    a.N = F;
+    a.n_tiles = F / (lmoe::kBN / 2);
+    a.kb1 = l / lmoe::kBK;
+    a.b_group_rows = F;
+    a.out = h->hb;
+    a.ldo = F;
+    a.hints = 1;
+    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, h->sms, s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 5, s);
+  // 5: grouped expert down-projection
+  {
+    GemmMaps m = h->m_expert_down;
+    m.a = mh;
+    GemmArgs a = base_args(h);
+    a.grouped = 1;
+    a.num_groups = E;
+    a.seg_offsets = h->offsets;
+    a.N = l;
+    a.n_tiles = ceil_div(l, lmoe::kBN);
+    a.kb1 = F / lmoe::kBK;
+    a.b_group_rows = l;
+    a.out = h->ob;
+    a.ldo = l;
+    a.hints = 1;
+    LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, h->sms, false, s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 6, s);
+  // 6: combine
+  LMOE_CK(h, lmoe::launch_combine(h->ob, h->gates, h->pos, Ti, k, l, h->cb, s));
+  h->launches += 1;
+  record(h, slot_base, 7, s);
+  // 7: shared expert gate+up on the full width
+  if (Fs > 0) {
+    GemmMaps m = h->m_shared;
+    m.a = mx;
+    GemmArgs a = base_args(h);
+    a.M = Ti;
+    a.N = Fs;
+    a.n_tiles = Fs / (lmoe::kBN / 2);
+    a.kb1 = dd / lmoe::kBK;
+    a.out = h->sh;
+    a.ldo = Fs;
+    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 8, s);
+  // 8: up-projection (+ shared expert's down-projection, K-concatenated)
+  {
+    GemmMaps m = h->m_up;
+    m.a = mc;
+    if (Fs > 0) m.a2 = msh; else m.a2 = mc;
+    GemmArgs a = base_args(h);
+    a.M = Ti;
+    a.N = dd;
+    a.n_tiles = ceil_div(dd, lmoe::kBN);
+    a.kb1 = l / lmoe::kBK;
+    a.kb2 = Fs / lmoe::kBK;
+    a.out = out;
+    a.ldo = dd;
+    const int grid = dense_grid(h, Ti, a.n_tiles);
+    if (out32)
+      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, Fs > 0, s));
+    else
+      LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, Fs > 0, s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 9, s);
+  h->last_T = T;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host, int64_t T,
+                           latentmoe_stream_t st) {
+  if (h == nullptr || x_host == nullptr || out_host == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const size_t x_bytes = static_cast<size_t>(T) * h->dims.hidden * 2;
+  const size_t y_bytes =
+      static_cast<size_t>(T) * h->dims.hidden * ((h->flags & LATENTMOE_OUT_FP32) ? 4 : 2);
+  if (h->x_stage == nullptr) {
+    LMOE_CK(h, cudaMalloc(&h->x_stage, static_cast<size_t>(h->dims.max_tokens) * h->dims.hidden * 2));
+    LMOE_CK(h, cudaMalloc(&h->y_stage, static_cast<size_t>(h->dims.max_tokens) * h->dims.hidden * 4));
+  }
+  LMOE_CK(h, cudaMemcpyAsync(h->x_stage, x_host, x_bytes, cudaMemcpyHostToDevice, s));
+  const int r = latentmoe_forward(h, h->x_stage, h->y_stage, T, st);
+  if (r != LATENTMOE_OK) return r;
+  LMOE_CK(h, cudaMemcpyAsync(out_host, h->y_stage, y_bytes, cudaMemcpyDeviceToHost, s));
+  LMOE_CK(h, cudaStreamSynchronize(s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_route_from_logits(latentmoe_t h, const float* logits, int64_t T, int32_t* idx,
+                                float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                int32_t* pos, latentmoe_stream_t st) {
+  if (h == nullptr || logits == nullptr || idx == nullptr || gates == nullptr)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const int r = run_routing(h, logits, static_cast<int>(T), s, 0);
+  if (r != LATENTMOE_OK) return r;
+  const size_t S = static_cast<size_t>(T) * h->k;
+  const size_t E = static_cast<size_t>(h->dims.num_experts);
+  LMOE_CK(h, cudaMemcpyAsync(idx, h->idx, S * 4, cudaMemcpyDeviceToDevice, s));
+  LMOE_CK(h, cudaMemcpyAsync(gates, h->gates, S * 4, cudaMemcpyDeviceToDevice, s));
+  if (counts) LMOE_CK(h, cudaMemcpyAsync(counts, h->counts, E * 4, cudaMemcpyDeviceToDevice, s));
+  if (offsets)
+    LMOE_CK(h, cudaMemcpyAsync(offsets, h->offsets, (E + 1) * 4, cudaMemcpyDeviceToDevice, s));
+  if (perm) LMOE_CK(h, cudaMemcpyAsync(perm, h->perm, S * 4, cudaMemcpyDeviceToDevice, s));
+  if (pos) LMOE_CK(h, cudaMemcpyAsync(pos, h->pos, S * 4, cudaMemcpyDeviceToDevice, s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_routing(latentmoe_t h, float* logits, int32_t* idx, float* gates,
+                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos,
+                          latentmoe_stream_t st) {
+  if (h == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (h->last_T == 0) return LATENTMOE_ERR_NOT_LOADED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const size_t T = static_cast<size_t>(h->last_T);
+  const size_t S = T * h->k;
+  const size_t E = static_cast<size_t>(h->dims.num_experts);
+  const auto dd = cudaMemcpyDeviceToDevice;
+  if (logits) LMOE_CK(h, cudaMemcpyAsync(logits, h->logits, T * E * 4, dd, s));
+  if (idx) LMOE_CK(h, cudaMemcpyAsync(idx, h->idx, S * 4, dd, s));
+  if (gates) LMOE_CK(h, cudaMemcpyAsync(gates, h->gates, S * 4, dd, s));
+  if (counts) LMOE_CK(h, cudaMemcpyAsync(counts, h->counts, E * 4, dd, s));
+  if (offsets) LMOE_CK(h, cudaMemcpyAsync(offsets, h->offsets, (E + 1) * 4, dd, s));
+  if (perm) LMOE_CK(h, cudaMemcpyAsync(perm, h->perm, S * 4, dd, s));
+  if (pos) LMOE_CK(h, cudaMemcpyAsync(pos, h->pos, S * 4, dd, s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_status(latentmoe_t h, uint32_t* device_status) {
+  if (h == nullptr || device_status == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  unsigned v = 0;
+  LMOE_CK(h, cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
+  LMOE_CK(h, cudaMemset(h->status, 0, 4));
+  *device_status = v;
+  if (v & LATENTMOE_STATUS_TIMEOUT) return LATENTMOE_ERR_TIMEOUT;
+  if (v != 0) return LATENTMOE_ERR_DEVICE_STATUS;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_set_profiling(latentmoe_t h, int slots) {
+  if (h == nullptr || slots < 0 || slots > 4096) return LATENTMOE_ERR_INVALID_ARG;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  h->events.clear();
+  h->prof_slots = 0;
+  h->forwards = 0;
+  const size_t n = static_cast<size_t>(slots) * (kNumStages + 1);
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t ev;
+    LMOE_CK(h, cudaEventCreate(&ev));
+    h->events.push_back(ev);
+  }
+  h->prof_slots = slots;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count) {
+  if (h == nullptr || ms == nullptr || slot < 0 || slot >= h->prof_slots || count < 0)
+    return LATENTMOE_ERR_INVALID_ARG;
+  const int base = slot * (kNumStages + 1);
+  LMOE_CK(h, cudaEventSynchronize(h->events[base + kNumStages]));
+  for (int i = 0; i < count && i < kNumStages; ++i) {
+    float t = 0.0f;
+    LMOE_CK(h, cudaEventElapsedTime(&t, h->events[base + i], h->events[base + i + 1]));
+    ms[i] = t;
+  }
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches) {
+  if (h == nullptr || launches == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  *launches = h->launches;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_last_cuda_error(latentmoe_t h) { return h ? h->last_cuda : 0; }
+
+// ---------------------------------------------------------------- debug GEMM
+int latentmoe_debug_status(uint32_t* device_status);
+
+namespace {
+unsigned* debug_status_word() {
+  static unsigned* p = nullptr;
+  if (p == nullptr) {
+    if (cudaMalloc(&p, 16) != cudaSuccess) return nullptr;
+    cudaMemset(p, 0, 16);
+  }
+  return p;
+}
+
+int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offsets, int64_t G,
+                    int64_t M, int64_t N, int64_t K, int mode, cudaStream_t s) {
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || mode < 0 || mode > 2)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (K % 128 || (mode != 1 && N % 128) || M > (1 << 30) || N > (1 << 20))
+    return LATENTMOE_ERR_UNSUPPORTED;
+  if (offsets && (G < 1 || G > lmoe::kMaxGroups)) return LATENTMOE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return LATENTMOE_ERR_UNSUPPORTED;
+  unsigned* status = debug_status_word();
+  if (status == nullptr) return LATENTMOE_ERR_CUDA;
+  const int64_t groups = offsets ? G : 1;
+  GemmMaps m;
+  bool ok = make_map(&m.a, A, M, K, K, 128);
+  if (mode == 2) {
+    ok &= make_map(&m.b, B, groups * N, K, K, 128);
+    ok &= make_map(&m.bu, static_cast<const __nv_bfloat16*>(B) + groups * N * K, groups * N, K,
+                   K, 128);
+  } else {
+    ok &= make_map(&m.b, B, groups * N, K, K, 256);
+    m.bu = m.b;
+  }
+  if (!ok) return LATENTMOE_ERR_CUDA;
+  m.a2 = m.a;
+  m.b2 = m.b;
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.grouped = offsets ? 1 : 0;
+  a.num_groups = static_cast<int>(groups);
+  a.seg_offsets = offsets;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.n_tiles = mode == 2 ? static_cast<int>(N / 128) : ceil_div(N, lmoe::kBN);
+  a.kb1 = static_cast<int>(K / lmoe::kBK);
+  a.b_group_rows = static_cast<int>(N);
+  a.group_m = 16;
+  a.out = C;
+  a.ldo = N;
+  a.status = status;
+  const long long tiles = static_cast<long long>(ceil_div(M, lmoe::kBM)) * a.n_tiles;
+  const int grid = offsets ? num_sms() : static_cast<int>(tiles < num_sms() ? tiles : num_sms());
+  cudaError_t e;
+  if (mode == 0) e = lmoe::launch_gemm_bf16(m, a, grid, false, s);
+  else if (mode == 1) e = lmoe::launch_gemm_f32(m, a, grid, false, s);
+  else e = lmoe::launch_gemm_swiglu(m, a, grid, s);
+  return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
+}
+}  // namespace
+
+int latentmoe_debug_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int mode, latentmoe_stream_t st) {
+  return debug_gemm_impl(A, B, C, nullptr, 1, M, N, K, mode, reinterpret_cast<cudaStream_t>(st));
+}
+
+int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C, const int32_t* offsets,
+                                 int64_t groups, int64_t M, int64_t N, int64_t K, int mode,
+                                 latentmoe_stream_t st) {
+  if (offsets == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  return debug_gemm_impl(A, B, C, offsets, groups, M, N, K, mode,
+                         reinterpret_cast<cudaStream_t>(st));
+}
+
+namespace {
+// One thread waits, with the library's bounded wait, on an mbarrier that
+// nothing ever arrives on; the wait gives up after limit_ns and records it.
+__global__ void wait_timeout_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    lmoe::mbar_init(&bar, 1);
+    abort_flag = 0;
+    lmoe::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) lmoe::wait_bounded(&bar, 0, &abort_flag, status, limit_ns);
+}
+}  // namespace
+
+int latentmoe_debug_wait_timeout(uint64_t limit_ns, uint32_t* device_status) {
+  if (device_status == nullptr || limit_ns > 1000000000ull) return LATENTMOE_ERR_INVALID_ARG;
+  unsigned* p = debug_status_word();
+  if (p == nullptr) return LATENTMOE_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32>>>(p, limit_ns);
+  if (cudaGetLastError() != cudaSuccess) return LATENTMOE_ERR_CUDA;
+  return latentmoe_debug_status(device_status);
+}
+
+int latentmoe_debug_status(uint32_t* device_status) {
+  if (device_status == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  unsigned* p = debug_status_word();
+  if (p == nullptr) return LATENTMOE_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LATENTMOE_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LATENTMOE_ERR_CUDA;
+  cudaMemset(p, 0, 4);
+  *device_status = v;
+  if (v & LATENTMOE_STATUS_TIMEOUT) return LATENTMOE_ERR_TIMEOUT;
+  return v ? LATENTMOE_ERR_DEVICE_STATUS : LATENTMOE_OK;
+}
+
+}  // extern "C"

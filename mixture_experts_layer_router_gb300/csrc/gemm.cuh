@@ -1,0 +1,415 @@
+// Persistent tcgen05 GEMM, D = A B^T, for every matrix product of the layer.
+//
+// A [rows, K] and B [N, K] are bf16, K-major (nn.Linear layout), read by TMA
+// into a ring of shared-memory stages with 128-byte swizzle. One thread
+// issues tcgen05.mma (M = 128, N = 256, K = 16 per instruction) into one of
+// two fp32 accumulators in tensor memory (2 x 256 columns); four epilogue
+// warps drain the other accumulator meanwhile, apply the epilogue and store.
+//
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator and MMA issuer (one lane)
+//   warps 2..5  epilogue; warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32)
+//
+// Tiles: dense GEMMs walk (m, n) in bands of `group_m` m-tiles so that
+// concurrent CTAs share A rows and B columns in L2. Grouped GEMMs (the
+// expert FFNs) take the expert segments [seg[g], seg[g+1]) of A's rows from
+// device memory; every CTA builds the prefix of m-tiles per group in shared
+// memory and walks (group, n, m) with m fastest, so the CTAs working on the
+// two or three m-tiles of one expert read each weight tile at about the same
+// time. No host synchronisation is needed to know the segment sizes.
+//
+// Epilogues:
+//   kEpiBf16     C[row, col] = bf16(acc)
+//   kEpiF32      C[row, col] = acc (+ bias[col])
+//   kEpiSwiglu   B holds 128 gate rows then 128 up rows of the same output
+//                features; C[row, f] = bf16(SiLU(gate) * up)
+//   kEpiScatter  token row t is written to rows pos[t*k + j], j < k, of C
+//
+// Ragged edges: rows past a segment or past M are computed on whatever TMA
+// brought in (zeros past the tensor) and never stored; columns past N are not
+// stored either.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace lmoe {
+
+enum EpiMode : int { kEpiBf16 = 0, kEpiF32 = 1, kEpiSwiglu = 2, kEpiScatter = 3 };
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kBK * 2;
+constexpr int kBTileBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kMaxGroups = 512;
+constexpr int kGemmThreads = 192;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kBarrierBytes = 8 * (2 * kStages + 2 + 2 + 1);
+constexpr int kGemmSmemBytes =
+    1024 /* alignment slack */ + kStages * kStageBytes + kBarrierBytes + 16 +
+    2 * (kMaxGroups + 1) * 4;
+
+struct GemmArgs {
+  int grouped;             // 0: dense rows [0, M); 1: segments from seg_offsets
+  int num_groups;          // G <= kMaxGroups (grouped)
+  const int* seg_offsets;  // [G+1] row offsets of the segments (grouped)
+  int M;                   // rows (dense)
+  int N;                   // output columns (kEpiSwiglu: output features)
+  int n_tiles;             // tiles along N
+  int kb1;                 // k-blocks of the first (A, B) pair
+  int kb2;                 // k-blocks of the second pair (dual-K only)
+  int b_group_rows;        // rows of B per group (grouped)
+  int group_m;             // dense raster band, in m-tiles
+  void* out;
+  long long ldo;           // row stride of out, elements
+  const float* bias;       // kEpiF32, may be null
+  const int* pos;          // kEpiScatter: [M * topk] destination rows (-1: skip)
+  int topk;
+  unsigned* status;        // device status word
+  int hints;               // bit 0: A tiles evict_last in L2; bit 1: B tiles evict_first
+};
+
+struct TileCoord {
+  int row0;  // first A row of the tile
+  int rows;  // valid rows (<= kBM)
+  int n;     // n-tile index
+  int brow;  // first B row
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int t, const GemmArgs& a, const int* seg_s,
+                                                 const int* mt_s, int b_rows_per_tile) {
+  TileCoord c;
+  if (a.grouped) {
+    // largest g with mt_s[g] * n_tiles <= t; that group is non-empty
+    int lo = 0, hi = a.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mt_s[mid] * a.n_tiles <= t) lo = mid; else hi = mid - 1;
+    }
+    const int g = lo;
+    const int mtg = mt_s[g + 1] - mt_s[g];
+    const int local = t - mt_s[g] * a.n_tiles;
+    const int n = local / mtg;
+    const int m = local - n * mtg;
+    const int seg0 = seg_s[g];
+    const int len = seg_s[g + 1] - seg0;
+    c.row0 = seg0 + m * kBM;
+    c.rows = min(kBM, len - m * kBM);
+    c.n = n;
+    c.brow = g * a.b_group_rows + n * b_rows_per_tile;
+  } else {
+    const int mt = (a.M + kBM - 1) / kBM;
+    const int per = a.group_m * a.n_tiles;
+    const int band = t / per;
+    const int first = band * a.group_m;
+    const int gm = min(a.group_m, mt - first);
+    const int local = t - band * per;
+    const int m = first + local % gm;
+    const int n = local / gm;
+    c.row0 = m * kBM;
+    c.rows = min(kBM, a.M - c.row0);
+    c.n = n;
+    c.brow = n * b_rows_per_tile;
+  }
+  return c;
+}
+
+// All lanes of a warp wait together: lane 0 polls, the verdict is broadcast,
+// then the other lanes observe the completed phase themselves.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = wait_bounded(bar, parity, abort_flag, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && lane != 0) ok = mbar_try_wait(bar, parity) ? 1 : wait_bounded(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&v)[32],
+                                            long long row, int col) {
+  if constexpr (MODE == kEpiF32) {
+    float* dst = reinterpret_cast<float*>(a.out) + row * a.ldo + col;
+    if (col + 32 <= a.N && (a.ldo & 3) == 0) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float4 f;
+        f.x = __uint_as_float(v[i + 0]);
+        f.y = __uint_as_float(v[i + 1]);
+        f.z = __uint_as_float(v[i + 2]);
+        f.w = __uint_as_float(v[i + 3]);
+        if (a.bias != nullptr) {
+          f.x += a.bias[col + i + 0];
+          f.y += a.bias[col + i + 1];
+          f.z += a.bias[col + i + 2];
+          f.w += a.bias[col + i + 3];
+        }
+        *reinterpret_cast<float4*>(dst + i) = f;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (col + i < a.N) {
+          float f = __uint_as_float(v[i]);
+          if (a.bias != nullptr) f += a.bias[col + i];
+          dst[i] = f;
+        }
+      }
+    }
+  } else {
+    uint4 p[4];
+    uint32_t* pw = reinterpret_cast<uint32_t*>(p);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pw[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    if constexpr (MODE == kEpiScatter) {
+      for (int j = 0; j < a.topk; ++j) {
+        const int dst_row = a.pos[row * a.topk + j];
+        if (dst_row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                              static_cast<long long>(dst_row) * a.ldo + col);
+        dst[0] = p[0]; dst[1] = p[1]; dst[2] = p[2]; dst[3] = p[3];
+      }
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                            row * a.ldo + col);
+      dst[0] = p[0]; dst[1] = p[1]; dst[2] = p[2]; dst[3] = p[3];
+    }
+  }
+}
+
+template <int MODE, bool DUAL>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmBu,
+                   const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB2, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* done_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
+  int* mt_s = seg_s + kMaxGroups + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kBRowsPerTile = (MODE == kEpiSwiglu) ? kBN / 2 : kBN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (MODE == kEpiSwiglu) tma_prefetch_desc(&tmBu);
+    if (DUAL) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (a.grouped) {
+    for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
+  }
+  __syncthreads();
+  if (a.grouped && warp == 2) {
+    // exclusive prefix of ceil(n_g / kBM) over the groups
+    int carry = 0;
+    if (lane == 0) mt_s[0] = 0;
+    for (int base = 0; base < a.num_groups; base += 32) {
+      const int g = base + lane;
+      int v = 0;
+      if (g < a.num_groups) {
+        const int len = seg_s[g + 1] - seg_s[g];
+        v = len > 0 ? (len + kBM - 1) / kBM : 0;
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (g < a.num_groups) mt_s[g + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles =
+      a.grouped ? mt_s[a.num_groups] * a.n_tiles : ((a.M + kBM - 1) / kBM) * a.n_tiles;
+  const int kb_total = a.kb1 + (DUAL ? a.kb2 : 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint64_t pol = (a.hints & 1) ? policy_evict_last() : policy_evict_normal();
+      const uint64_t pol_b = (a.hints & 2) ? policy_evict_first() : policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0;
+      uint32_t issued_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const TileCoord c = decode_tile(t, a, seg_s, mt_s, kBRowsPerTile);
+        for (int kb = 0; kb < kb_total; ++kb) {
+          if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = tiles + stage * kStageBytes;
+          uint8_t* sb = sa + kATileBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          if (!DUAL || kb < a.kb1) {
+            const int kc = kb * kBK;
+            tma_load_2d(&tmA, &full_bar[stage], sa, kc, c.row0, pol);
+            if (MODE == kEpiSwiglu) {
+              tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
+              tma_load_2d(&tmBu, &full_bar[stage], sb + kBTileBytes / 2, kc, c.brow, pol_b);
+            } else {
+              tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
+            }
+          } else {
+            const int kc = (kb - a.kb1) * kBK;
+            tma_load_2d(&tmA2, &full_bar[stage], sa, kc, c.row0, pol);
+            tma_load_2d(&tmB2, &full_bar[stage], sb, kc, c.brow, pol_b);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this thread started lands before the CTA may exit
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = instr_desc_bf16(kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        if (!wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < kb_total; ++kb) {
+          if (!wait_bounded(&full_bar[stage], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint8_t* sa = tiles + stage * kStageBytes;
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + kATileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // +32 bytes along K inside the 128-byte swizzled row = +2 in addr>>4
+            tc_mma(d_tmem, da + 2ull * k, db + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      tc_commit(done_bar);
+      wait_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const TileCoord c = decode_tile(t, a, seg_s, mt_s, kBRowsPerTile);
+      if (!warp_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, a.status)) break;
+      tc_fence_after_sync();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      const bool row_ok = r < c.rows;
+      const long long row = static_cast<long long>(c.row0) + r;
+      if constexpr (MODE == kEpiSwiglu) {
+#pragma unroll 1
+        for (int ch = 0; ch < kBN / 64; ++ch) {
+          uint32_t g[32], u[32];
+          tmem_ld_32cols(tbase + ch * 32, g);
+          tmem_ld_32cols(tbase + kBN / 2 + ch * 32, u);
+          tmem_ld_wait();
+          const int col = c.n * (kBN / 2) + ch * 32;
+          if (row_ok && col < a.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              g[i] = __float_as_uint(silu(__uint_as_float(g[i])) * __uint_as_float(u[i]));
+            store_chunk<kEpiBf16>(a, g, row, col);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < kBN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32cols(tbase + ch * 32, v);
+          tmem_ld_wait();
+          const int col = c.n * kBN + ch * 32;
+          if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace lmoe

@@ -1,0 +1,42 @@
+// Host-side launchers of the library's kernels (internal interface).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gemm.cuh"
+
+namespace lmoe {
+
+struct GemmMaps {
+  CUtensorMap a, b, bu, a2, b2;
+};
+
+// One launch of gemm_tc_kernel<MODE, DUAL>; `grid` persistent CTAs.
+cudaError_t launch_gemm_bf16(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
+                             cudaStream_t s);
+cudaError_t launch_gemm_f32(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
+                            cudaStream_t s);
+cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+
+// Softmax over E and stable top-k per token: idx [T,k] int32, gates [T,k].
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
+                              float* gates, cudaStream_t s);
+
+// Counting sort of the T*k slots by expert. Scratch: cnt and cbase, each
+// sort_scratch_ints(S, E) ints. Three launches.
+constexpr int kSortChunk = 1024;
+inline long long sort_scratch_ints(long long S, long long E) {
+  return ((S + kSortChunk - 1) / kSortChunk) * E;
+}
+cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbase, int* counts,
+                        int* offsets, int* perm, int* pos, unsigned* status, cudaStream_t s);
+constexpr int kSortLaunches = 3;
+
+// c[t] = sum_j gates[t,j] * o[pos[t,j]] in fp32, j order; bf16 out.
+cudaError_t launch_combine(const __nv_bfloat16* o, const float* gates, const int* pos, int T,
+                           int k, int l, __nv_bfloat16* c, cudaStream_t s);
+
+}  // namespace lmoe

@@ -1,0 +1,247 @@
+// Routing: softmax gating with stable top-k, and the counting sort of the
+// (token, choice) slots by expert.
+//
+// "The Training and RL Infrastructure Behind MAI-Thinking-1": the router
+// reads the full hidden state and gates with a softmax (section "The model
+// the systems run"); top-k uses a stable sort so equal logits always resolve
+// to the lower expert index (section "Bitwise determinism"); dropless routing
+// with token metadata kept on the device (sections "Sharding and
+// parallelism" and, in "Frontier Pre-training at Microsoft AI", "Reducing
+// per-expert overhead").
+//
+// Everything here is integer or fixed-order: no floating-point atomics, so
+// the outputs are bitwise reproducible.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+// One warp per token. Lane i holds logits of experts i, i+32, ... (VPL of
+// them). Softmax: max and sum of exp by warp butterflies (fixed order).
+// Selection: k rounds of a warp arg-max under the order (value desc, index
+// asc); the winner is marked taken. NaN logits are treated as -inf.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int renorm,
+                                                         int* __restrict__ idx,
+                                                         float* __restrict__ gates) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + static_cast<long long>(t) * E;
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    float x = (e < E) ? row[e] : -INFINITY;
+    v[i] = (x != x) ? -INFINITY : x;
+  }
+  float m = v[0];
+#pragma unroll
+  for (int i = 1; i < VPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+
+  uint32_t taken = 0;
+  float gsel[16];
+  int isel[16];
+  float gsum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < k) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float g = expf(bv - m) / s;
+      gsel[j] = g;
+      isel[j] = bi;
+      gsum += g;
+    }
+  }
+  if (lane == 0) {
+    const float scale = renorm ? 1.0f / gsum : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < k) {
+        idx[static_cast<long long>(t) * k + j] = isel[j];
+        gates[static_cast<long long>(t) * k + j] = renorm ? gsel[j] * scale : gsel[j];
+      }
+    }
+  }
+}
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
+                              float* gates, cudaStream_t s) {
+  const int blocks = (T + 7) / 8;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+  else if (vpl <= 2)
+    route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+  else if (vpl <= 4)
+    route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+  else if (vpl <= 8)
+    route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+  else
+    route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Counting sort. The S = T*k slots s (flattened [T, k], token t = s / k) are
+// cut into chunks of kSortChunk. (1) Each chunk counts its experts into row
+// b of cnt [chunks, E]. (2) For each expert, an exclusive scan over chunks
+// gives cbase[b, e]; counts[e] is the total, offsets the exclusive scan over
+// experts. (3) Each chunk walks its slots in order, 32 at a time; lanes with
+// the same expert get consecutive ranks in lane order, so slot order inside
+// an expert follows s, i.e. token order (a token never picks an expert
+// twice). Expert ids outside [0, E) set kStatusBadExpert and get pos = -1.
+
+__global__ void __launch_bounds__(256) sort_hist_kernel(const int* __restrict__ idx, int S, int E,
+                                                        int* __restrict__ cnt, unsigned* status) {
+  extern __shared__ int hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kSortChunk;
+  bool bad = false;
+  for (int i = threadIdx.x; i < kSortChunk; i += blockDim.x) {
+    const int s = base + i;
+    if (s < S) {
+      const int e = idx[s];
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+        atomicAdd(&hist[e], 1);
+      else
+        bad = true;
+    }
+  }
+  if (bad) atomicOr(status, kStatusBadExpert);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    cnt[static_cast<long long>(blockIdx.x) * E + i] = hist[i];
+}
+
+// One block of 512 threads; thread e owns expert e (E <= 512).
+__global__ void __launch_bounds__(512) sort_scan_kernel(const int* __restrict__ cnt, int nb, int E,
+                                                        int* __restrict__ cbase,
+                                                        int* __restrict__ counts,
+                                                        int* __restrict__ offsets) {
+  __shared__ int warp_tot[16];
+  const int e = threadIdx.x;
+  const int lane = e & 31, w = e >> 5;
+  int run = 0;
+  if (e < E) {
+    int b = 0;
+    for (; b + 8 <= nb; b += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = cnt[static_cast<long long>(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cbase[static_cast<long long>(b + i) * E + e] = run;
+        run += v[i];
+      }
+    }
+    for (; b < nb; ++b) {
+      const int v = cnt[static_cast<long long>(b) * E + e];
+      cbase[static_cast<long long>(b) * E + e] = run;
+      run += v;
+    }
+  }
+  // exclusive scan of run over e
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int i = 0; i < w; ++i) wbase += warp_tot[i];
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = wbase + incl - run;
+    if (e == E - 1) offsets[E] = wbase + incl;
+  }
+}
+
+// One warp per chunk.
+__global__ void __launch_bounds__(32) sort_scatter_kernel(const int* __restrict__ idx, int S, int k,
+                                                          int E, const int* __restrict__ cbase,
+                                                          const int* __restrict__ offsets,
+                                                          int* __restrict__ perm,
+                                                          int* __restrict__ pos) {
+  extern __shared__ int run[];
+  const int lane = threadIdx.x;
+  for (int i = lane; i < E; i += 32)
+    run[i] = offsets[i] + cbase[static_cast<long long>(blockIdx.x) * E + i];
+  const int base = blockIdx.x * kSortChunk;
+  int ev[kSortChunk / 32];
+#pragma unroll
+  for (int st = 0; st < kSortChunk / 32; ++st) {
+    const int s = base + st * 32 + lane;
+    ev[st] = (s < S) ? idx[s] : -1;
+  }
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int st = 0; st < kSortChunk / 32; ++st) {
+    const int s = base + st * 32 + lane;
+    const int e = ev[st];
+    const bool valid = s < S && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const int key = valid ? e : (0x40000000 | lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & lt);
+    if (valid) {
+      const int slot = run[e] + rank;
+      perm[slot] = s / k;
+      pos[s] = slot;
+    } else if (s < S) {
+      pos[s] = -1;
+    }
+    __syncwarp();
+    if (valid && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbase, int* counts,
+                        int* offsets, int* perm, int* pos, unsigned* status, cudaStream_t s) {
+  const int nb = (S + kSortChunk - 1) / kSortChunk;
+  const size_t smem = static_cast<size_t>(E) * sizeof(int);
+  sort_hist_kernel<<<nb, 256, smem, s>>>(idx, S, E, cnt, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  sort_scan_kernel<<<1, 512, 0, s>>>(cnt, nb, E, cbase, counts, offsets);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  sort_scatter_kernel<<<nb, 32, smem, s>>>(idx, S, k, E, cbase, offsets, perm, pos);
+  return cudaGetLastError();
+}
+
+}  // namespace lmoe

@@ -1,0 +1,150 @@
+"""The whole layer on the GPU against the float64 oracle, on the small
+configs in full (tiny, mid, imbalanced) and on flag variants.
+
+Output parity routes the oracle from the GPU's own fp32 logits (exported by
+latentmoe_get_routing), because near-equal logits can legitimately pick a
+different expert in float64; the logits themselves are checked separately.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_router_gb300 import capi, synth
+import gpu_helpers as gh
+from oracle import latentmoe_ref as ref
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(name, seed=0, bias_override=None):
+    cfg = synth.CONFIGS[name]
+    w = synth.make_weights(cfg, seed, "cuda")
+    if bias_override is not None:
+        w["b_r"] = bias_override
+    x = synth.make_x(cfg, seed, "cuda")
+    return cfg, w, x
+
+
+def _check_layer(cfg, w, x, layer, T=None):
+    T = cfg.T if T is None else T
+    y = layer.forward(x[:T])
+    r = layer.get_routing(T, "cuda")
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    W = gh.oracle_weights(w)
+    xs = gh.f64(x[:T])
+    # logits: GPU fp32 vs float64
+    L_ref = ref.router_logits(xs, W.w_r, W.b_r)
+    L_gpu = gh.f64(r["logits"])
+    assert np.abs(L_gpu - L_ref).max() <= gh.LOGIT_MAX_ABS
+    # routing from the GPU logits: bit-exact integers
+    renorm = bool(layer.flags & capi.RENORM)
+    ora = ref.forward(xs, W, cfg.k, renorm=renorm, logits=L_gpu)
+    gh.assert_routing_equal(r, ora, T, cfg.k)
+    rel, mx = gh.assert_y_close(y, ora["y"])
+    return y, ora
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "imbalanced"])
+def test_forward_matches_oracle(name):
+    cfg, w, x = _setup(name)
+    layer = gh.make_layer(cfg, w)
+    _check_layer(cfg, w, x, layer)
+
+
+def test_tiny_flag_variants():
+    cfg, w, x = _setup("tiny", seed=3)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(4)
+    w["b_r"] = (torch.randn(cfg.E, generator=g) * 0.5).cuda()
+    for renorm in (False, True):
+        for out_fp32 in (False, True):
+            layer = gh.make_layer(cfg, w, renorm=renorm, out_fp32=out_fp32)
+            y, _ = _check_layer(cfg, w, x, layer)
+            assert y.dtype == (torch.float32 if out_fp32 else torch.bfloat16)
+
+
+def test_ragged_token_counts():
+    """T not a multiple of the 128-row tile, and T = 1."""
+    cfg, w, x = _setup("tiny", seed=5)
+    layer = gh.make_layer(cfg, w)
+    for T in (1, 77, 128):
+        _check_layer(cfg, w, x, layer, T=T)
+
+
+def test_shared_expert_small():
+    """A small layer with a shared expert (the MAI-Base-2 structure)."""
+    cfg = synth.LayerConfig("tiny-shared", T=200, d=256, l=128, E=8, k=3, F=256, Fs=384)
+    w = synth.make_weights(cfg, 7, "cuda")
+    x = synth.make_x(cfg, 7, "cuda")
+    layer = gh.make_layer(cfg, w)
+    _check_layer(cfg, w, x, layer)
+
+
+def test_zero_input_routes_to_first_experts():
+    cfg, w, x = _setup("tiny", seed=8)
+    x = torch.zeros_like(x)
+    layer = gh.make_layer(cfg, w)
+    y = layer.forward(x)
+    r = layer.get_routing(cfg.T, "cuda")
+    torch.cuda.synchronize()
+    assert torch.all(r["idx"].cpu() == torch.arange(cfg.k, dtype=torch.int32)[None, :])
+    counts = r["counts"].cpu()
+    assert counts[:cfg.k].tolist() == [cfg.T] * cfg.k and counts[cfg.k:].sum() == 0
+    assert torch.all(y == 0)
+
+
+def test_forward_is_bitwise_deterministic():
+    cfg, w, x = _setup("imbalanced", seed=1)
+    layer = gh.make_layer(cfg, w)
+    a = layer.forward(x).clone()
+    b = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_forward_host_matches_device_forward():
+    cfg, w, x = _setup("mid", seed=2)
+    layer = gh.make_layer(cfg, w)
+    y_dev = layer.forward(x)
+    torch.cuda.synchronize()
+    xh = x.cpu().pin_memory()
+    yh = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(xh, yh)
+    assert torch.equal(yh, y_dev.cpu())
+
+
+def test_launch_count_and_stage_times():
+    cfg, w, x = _setup("tiny")
+    layer = gh.make_layer(cfg, w)
+    layer.set_profiling(2)
+    n0 = layer.launch_count()
+    layer.forward(x)
+    assert layer.launch_count() - n0 == 10
+    t = layer.stage_times(0)
+    assert set(t) == {"router_gemm", "route_topk", "sort", "down_proj", "expert_gate_up",
+                      "expert_down", "combine", "shared_gate_up", "up_proj"}
+    assert all(v >= 0 for v in t.values())
+
+
+def test_error_paths_on_device():
+    cfg, w, x = _setup("tiny")
+    gh.lib()
+    layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, 0, max_tokens=cfg.T)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    lib = capi.load()
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.latentmoe_forward(layer.handle, x.data_ptr(), y.data_ptr(), cfg.T, s) == \
+        capi.ERR_NOT_LOADED
+    layer.load_weights(w)
+    assert lib.latentmoe_forward(layer.handle, x.data_ptr(), y.data_ptr(), cfg.T + 1, s) == \
+        capi.ERR_INVALID_ARG
+    assert lib.latentmoe_forward(layer.handle, x.data_ptr(), y.data_ptr(), 0, s) == \
+        capi.ERR_INVALID_ARG
+    assert lib.latentmoe_forward(layer.handle, x.data_ptr() + 2, y.data_ptr(), cfg.T, s) == \
+        capi.ERR_UNSUPPORTED
+    w2 = dict(w)
+    w2["w_g"] = None
+    with pytest.raises(capi.LatentMoEError):
+        layer.load_weights(w2)
+    assert layer.status() == 0
