@@ -144,6 +144,33 @@ int latentmoe_route_from_logits(latentmoe_t h, const float* logits, int64_t T,
                                 int32_t* offsets, int32_t* perm, int32_t* pos,
                                 latentmoe_stream_t stream);
 
+/* Allocation-free routing. The pages have no counterpart to this entry; it
+ * exists for callers that cannot allocate device memory: an application
+ * whose own memory pool owns the whole device (where an extra cudaMalloc
+ * fails or breaks the pool's accounting), or a latency-critical loop that
+ * cannot pay for cudaFree's implicit device synchronisation.
+ * It computes exactly what latentmoe_route_from_logits computes, without a
+ * handle: from fp32 logits [T, E] (device), idx [T, k] int32, gates [T, k]
+ * fp32, counts [E], offsets [E+1], perm [T*k] and pos [T, k] int32, all
+ * device pointers supplied by the caller (none may be NULL; 4-byte aligned).
+ * flags may hold only LATENTMOE_RENORM. It allocates nothing: the scratch of
+ * the counting sort is one fixed device array inside the library (1 MiB plus
+ * 256 bytes, held by every GPU that loads the library until the process
+ * exits). Limits: 1 <= k <= 16, k <= E <= 512, and ceil(T*k / 1024) * E <=
+ * 131072 (for example T*k <= 262144 at E = 512); larger sizes return
+ * LATENTMOE_ERR_UNSUPPORTED before any work is enqueued.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the one array and it keeps the last call's
+ * contents: calls whose work overlaps on the GPU (two streams, or two host
+ * threads) race and must be serialised by the caller. Asynchronous on
+ * `stream`. */
+int latentmoe_route_from_logits_static(const float* logits, int64_t T, int64_t E,
+                                       int top_k, uint32_t flags, int32_t* idx,
+                                       float* gates, int32_t* counts,
+                                       int32_t* offsets, int32_t* perm, int32_t* pos,
+                                       latentmoe_stream_t stream);
+
 /* Copy the routing state of the last forward on this handle into caller
  * device buffers (each may be NULL): logits [T, E] fp32 (bias included),
  * idx, gates, counts, offsets, perm, pos as in latentmoe_route_from_logits.

@@ -53,6 +53,8 @@ SIGNATURES = {
     "latentmoe_forward_host": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "latentmoe_destroy": (ctypes.c_int, [_c_void_p]),
     "latentmoe_route_from_logits": (ctypes.c_int, [_c_void_p, _c_void_p, _i64] + [_c_void_p] * 7),
+    "latentmoe_route_from_logits_static": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_int,
+                                                          ctypes.c_uint32] + [_c_void_p] * 7),
     "latentmoe_get_routing": (ctypes.c_int, [_c_void_p] + [_c_void_p] * 7 + [_c_void_p]),
     "latentmoe_get_status": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "latentmoe_set_profiling": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
