@@ -30,7 +30,7 @@ if ROOT not in sys.path:
 METRIC = "LatentMoE bf16 fwd tokens/s at MAI-Base-1 shape; % of tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "expert_gate_up"
-GEMM_SRC = os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", "gemm.cuh")
+GEMM_SRC = os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", "gemm_grouped.cuh")
 
 
 # ---------------------------------------------------------------- arithmetic
@@ -120,11 +120,14 @@ class ClockSampler:
         samples = []
         for r in rows:
             try:
-                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                whole, _, frac = r[0].partition(".")
+                ts = time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + float("0." + (frac or "0"))
                 samples.append((ts, float(r[1]), float(r[2]), r[4:8]))
             except Exception:
                 continue
-        inside = [s for s in samples if t0 - 1.0 <= s[0] <= t1 + 1.0] or samples
+        inside = [s for s in samples if t0 <= s[0] <= t1]
+        if len(inside) < 3:
+            inside = [s for s in samples if t0 - 0.5 <= s[0] <= t1 + 0.5] or samples
         if not inside:
             return None
         mhz = sorted(s[1] for s in inside)
@@ -259,6 +262,11 @@ def run_ours(args, cfg, rank, world, dist):
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
                            router_bias=w["b_r"] is not None)
     layer.load_weights(w)
+    # the library holds its own (packed) copy; the expert weights the CPU
+    # baseline needs are regenerated from their per-expert seeds
+    for key in ("w_g", "w_u", "w_d"):
+        w[key] = None
+    torch.cuda.empty_cache()
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -390,11 +398,11 @@ def run_ours(args, cfg, rank, world, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mai-base-1")
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-tokens", type=int, default=48)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -106,12 +106,15 @@ enum {
 int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags,
                      latentmoe_t* out);
 
-/* Bind the weights (device pointers, layouts in latentmoe_weights). The
- * library does not copy them: they are used in place by every later forward,
- * so the caller keeps them alive and unchanged until latentmoe_destroy or
- * the next latentmoe_load_weights. Builds the TMA descriptors; enqueues no
- * GPU work. Errors: INVALID_ARG (NULL pointer that the dims or flags need),
- * UNSUPPORTED (pointer not 16-byte aligned). */
+/* Load the weights (device pointers, layouts in latentmoe_weights). The
+ * library copies them into memory it owns (one allocation of the weights'
+ * size, freed by latentmoe_destroy or the next load) and rewrites the expert
+ * weights into contiguous 128-row x 64-column tiles for its grouped GEMMs.
+ * Synchronises the device before and after the copy, so pending writes to
+ * the caller's buffers are seen and the caller may free or reuse them as
+ * soon as this returns. Errors: INVALID_ARG (NULL pointer that the dims or
+ * flags need), UNSUPPORTED (pointer not 16-byte aligned), OUT_OF_MEMORY,
+ * CUDA. On error the handle has no weights loaded. */
 int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w);
 
 /* The layer forward. x: device bf16 [T, d]; out: device [T, d], bf16 (fp32

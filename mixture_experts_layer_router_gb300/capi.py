@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Dict, Optional
+from typing import Dict, Optional  # noqa: F401
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "liblatentmoe.so")
@@ -118,12 +118,9 @@ def _stream(stream) -> Optional[int]:
 
 
 class LatentMoE:
-    """A handle plus the torch tensors it borrows.
-
-    ``weights`` is a dict as made by ``synth.make_weights`` (device bf16
-    tensors, ``b_r`` fp32 or None). The tensors are kept referenced here
-    because the library uses them in place.
-    """
+    """A handle on one layer. ``load_weights`` takes a dict as made by
+    ``synth.make_weights`` (device bf16 tensors, ``b_r`` fp32 or None); the
+    library copies them, so the caller may drop its tensors afterwards."""
 
     def __init__(self, d: int, l: int, E: int, k: int, F: int, Fs: int = 0,
                  max_tokens: int = 1, renorm: bool = False, router_bias: bool = False,
@@ -137,7 +134,6 @@ class LatentMoE:
         check(lib.latentmoe_create(ctypes.byref(self.dims), k, self.flags, ctypes.byref(h)),
               "latentmoe_create")
         self.handle = h
-        self._weights: Dict[str, object] = {}
 
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
@@ -156,7 +152,6 @@ class LatentMoE:
                                   "w_gs", "w_us", "w_ds")))
         check(load().latentmoe_load_weights(self.handle, ctypes.byref(lw)),
               "latentmoe_load_weights")
-        self._weights = dict(w)
 
     def forward(self, x, out=None, stream=None):
         import torch

@@ -58,16 +58,38 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor [rows, cols] (row stride `ld` elements) read in boxes of
 // 64 columns x box_rows rows with 128-byte swizzle; out-of-range reads are 0.
 bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
-              uint32_t box_rows) {
+              uint32_t box_rows, uint32_t box_cols = 64) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {ld * 2};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token rows for the grouped kernel: boxes of kGTokBox rows x kGBK columns.
+bool make_token_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols) {
+  return make_map(map, ptr, rows, cols, cols, lmoe::kGTokBox, lmoe::kGBK);
+}
+
+// Packed weight tiles (see pack.cu): `tiles` contiguous blocks of 128 rows x
+// kGBK bf16, read one whole tile per box with the grouped kernel's swizzle.
+bool make_tile_map(CUtensorMap* map, const void* ptr, uint64_t tiles) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || tiles == 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(lmoe::kGBK), 128, tiles};
+  const cuuint64_t strides[2] = {lmoe::kGBK * 2, 128 * lmoe::kGBK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(lmoe::kGBK), 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      lmoe::kGBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -95,8 +117,10 @@ struct latentmoe {
   int device = 0;
   int sms = 1;
   bool loaded = false;
-  latentmoe_weights w;
-  GemmMaps m_router, m_down, m_gate_up, m_expert_down, m_shared, m_up;
+  latentmoe_weights w;          // the library-owned copies below
+  void* wmem = nullptr;          // one allocation holding every weight copy
+  GemmMaps m_router, m_down, m_shared, m_up;
+  CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
   // workspace
   void* ws = nullptr;
   float* logits = nullptr;
@@ -290,6 +314,7 @@ int latentmoe_destroy(latentmoe_t h) {
   if (h->x_stage) cudaFree(h->x_stage);
   if (h->y_stage) cudaFree(h->y_stage);
   if (h->ws) cudaFree(h->ws);
+  if (h->wmem) cudaFree(h->wmem);
   delete h;
   return LATENTMOE_OK;
 }
@@ -312,31 +337,91 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   LMOE_CK(h, cudaSetDevice(h->device));
 
   const uint64_t E = d.num_experts, dd = d.hidden, l = d.latent, F = d.ffn, Fs = d.shared_ffn;
-  bool ok = true;
-  ok &= make_map(&h->m_router.b, w->w_r, E, dd, dd, 256);
-  ok &= make_map(&h->m_down.b, w->w_dn, l, dd, dd, 256);
-  ok &= make_map(&h->m_gate_up.b, w->w_g, E * F, l, l, 128);
-  ok &= make_map(&h->m_gate_up.bu, w->w_u, E * F, l, l, 128);
-  ok &= make_map(&h->m_expert_down.b, w->w_d, E * l, F, F, 256);
-  ok &= make_map(&h->m_up.b, w->w_up, dd, l, l, 256);
+  // layout of the owned copy: dense weights as given, expert weights packed
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 1024);
+    return o;
+  };
+  const size_t o_r = take(E * dd * 2), o_b = take(bias ? E * 4 : 16), o_dn = take(l * dd * 2);
+  const size_t o_up = take(dd * l * 2);
+  const size_t o_g = take(E * F * l * 2), o_u = take(E * F * l * 2), o_d = take(E * l * F * 2);
+  const size_t o_gs = take(shared ? Fs * dd * 2 : 16), o_us = take(shared ? Fs * dd * 2 : 16);
+  const size_t o_ds = take(shared ? dd * Fs * 2 : 16);
+  // the caller's writes to its weights may still be in flight on any stream
+  LMOE_CK(h, cudaDeviceSynchronize());
+  h->loaded = false;
+  if (h->wmem) {
+    cudaFree(h->wmem);
+    h->wmem = nullptr;
+  }
+  {
+    const cudaError_t e = cudaMalloc(&h->wmem, off);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->wmem = nullptr;
+      return fail_cuda(h, e);
+    }
+  }
+  char* base = static_cast<char*>(h->wmem);
+  latentmoe_weights o;
+  memset(&o, 0, sizeof(o));
+  o.w_r = base + o_r;
+  o.b_r = bias ? reinterpret_cast<const float*>(base + o_b) : nullptr;
+  o.w_dn = base + o_dn;
+  o.w_up = base + o_up;
+  o.w_g = base + o_g;
+  o.w_u = base + o_u;
+  o.w_d = base + o_d;
   if (shared) {
-    ok &= make_map(&h->m_shared.b, w->w_gs, Fs, dd, dd, 128);
-    ok &= make_map(&h->m_shared.bu, w->w_us, Fs, dd, dd, 128);
-    ok &= make_map(&h->m_up.b2, w->w_ds, dd, Fs, Fs, 256);
+    o.w_gs = base + o_gs;
+    o.w_us = base + o_us;
+    o.w_ds = base + o_ds;
+  }
+  const auto dd2d = cudaMemcpyDeviceToDevice;
+  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_r), w->w_r, E * dd * 2, dd2d));
+  if (bias) LMOE_CK(h, cudaMemcpy(const_cast<float*>(o.b_r), w->b_r, E * 4, dd2d));
+  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_dn), w->w_dn, l * dd * 2, dd2d));
+  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_up), w->w_up, dd * l * 2, dd2d));
+  if (shared) {
+    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_gs), w->w_gs, Fs * dd * 2, dd2d));
+    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_us), w->w_us, Fs * dd * 2, dd2d));
+    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_ds), w->w_ds, dd * Fs * 2, dd2d));
+  }
+  typedef const __nv_bfloat16* cbf;
+  typedef __nv_bfloat16* mbf;
+  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_g), const_cast<mbf>(static_cast<cbf>(o.w_g)),
+                                     static_cast<long long>(E * F), static_cast<int>(l), h->sms, 0));
+  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_u), const_cast<mbf>(static_cast<cbf>(o.w_u)),
+                                     static_cast<long long>(E * F), static_cast<int>(l), h->sms, 0));
+  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_d), const_cast<mbf>(static_cast<cbf>(o.w_d)),
+                                     static_cast<long long>(E * l), static_cast<int>(F), h->sms, 0));
+  LMOE_CK(h, cudaDeviceSynchronize());
+
+  bool ok = true;
+  ok &= make_map(&h->m_router.b, o.w_r, E, dd, dd, 256);
+  ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
+  ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l / lmoe::kGBK));
+  ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l / lmoe::kGBK));
+  ok &= make_tile_map(&h->m_wd, o.w_d, E * l / 128 * (F / lmoe::kGBK));
+  ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 256);
+  if (shared) {
+    ok &= make_map(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
+    ok &= make_map(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
+    ok &= make_map(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
   }
   if (!ok) return LATENTMOE_ERR_CUDA;
   // unused map slots still travel as kernel parameters: give them a valid copy
   h->m_router.bu = h->m_router.a2 = h->m_router.b2 = h->m_router.b;
   h->m_down.bu = h->m_down.a2 = h->m_down.b2 = h->m_down.b;
-  h->m_gate_up.a2 = h->m_gate_up.b2 = h->m_gate_up.b;
-  h->m_expert_down.bu = h->m_expert_down.a2 = h->m_expert_down.b2 = h->m_expert_down.b;
   if (shared) {
     h->m_shared.a2 = h->m_shared.b2 = h->m_shared.b;
   } else {
     h->m_up.b2 = h->m_up.b;
   }
   h->m_up.bu = h->m_up.b;
-  h->w = *w;
+  h->w = o;
   h->loaded = true;
   return LATENTMOE_OK;
 }
@@ -358,8 +443,8 @@ int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latent
   // activation maps for this call
   CUtensorMap mx, mzp, mh, mc, msh;
   bool ok = make_map(&mx, x, T, dd, dd, 128);
-  ok &= make_map(&mzp, h->zp, S, l, l, 128);
-  ok &= make_map(&mh, h->hb, S, F, F, 128);
+  ok &= make_token_map(&mzp, h->zp, S, l);
+  ok &= make_token_map(&mh, h->hb, S, F);
   ok &= make_map(&mc, h->cb, T, l, l, 128);
   if (Fs > 0) ok &= make_map(&msh, h->sh, T, Fs, Fs, 128);
   if (!ok) return LATENTMOE_ERR_CUDA;
@@ -408,41 +493,37 @@ int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latent
     h->launches += 1;
   }
   record(h, slot_base, 4, s);
-  // 4: grouped gate+up with SwiGLU
+  // 4: grouped gate+up with SwiGLU (weights on the M side, tokens on N)
   {
-    GemmMaps m = h->m_gate_up;
-    m.a = mzp;
-    GemmArgs a = base_args(h);
-    a.grouped = 1;
+    lmoe::GroupedArgs a;
+    memset(&a, 0, sizeof(a));
     a.num_groups = E;
     a.seg_offsets = h->offsets;
-    a.N = F;
-    a.n_tiles = F / (lmoe::kBN / 2);
-    a.kb1 = l / lmoe::kBK;
-    a.b_group_rows = F;
+    a.fblocks = F / 128;
+    a.kb = l / lmoe::kGBK;
+    a.w_group_rows = F;
+    a.n_out = F;
     a.out = h->hb;
     a.ldo = F;
-    a.hints = 1;
-    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, h->sms, s));
+    a.status = h->status;
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, mzp, h->m_wg, h->m_wu, a, h->sms, s));
     h->launches += 1;
   }
   record(h, slot_base, 5, s);
   // 5: grouped expert down-projection
   {
-    GemmMaps m = h->m_expert_down;
-    m.a = mh;
-    GemmArgs a = base_args(h);
-    a.grouped = 1;
+    lmoe::GroupedArgs a;
+    memset(&a, 0, sizeof(a));
     a.num_groups = E;
     a.seg_offsets = h->offsets;
-    a.N = l;
-    a.n_tiles = ceil_div(l, lmoe::kBN);
-    a.kb1 = F / lmoe::kBK;
-    a.b_group_rows = l;
+    a.fblocks = ceil_div(l, 256);
+    a.kb = F / lmoe::kGBK;
+    a.w_group_rows = l;
+    a.n_out = l;
     a.out = h->ob;
     a.ldo = l;
-    a.hints = 1;
-    LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, h->sms, false, s));
+    a.status = h->status;
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, mh, h->m_wd, h->m_wd, a, h->sms, s));
     h->launches += 1;
   }
   record(h, slot_base, 6, s);
@@ -630,6 +711,48 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
   unsigned* status = debug_status_word();
   if (status == nullptr) return LATENTMOE_ERR_CUDA;
   const int64_t groups = offsets ? G : 1;
+  if (offsets && mode != 1) {
+    // the grouped kernel reads packed weight tiles: pack B into a temporary
+    const long long brows = groups * N * (mode == 2 ? 2 : 1);
+    __nv_bfloat16* bp = nullptr;
+    if (cudaMalloc(&bp, brows * K * 2) != cudaSuccess) {
+      cudaGetLastError();
+      return LATENTMOE_ERR_OUT_OF_MEMORY;
+    }
+    if (lmoe::launch_pack_tiles(static_cast<const __nv_bfloat16*>(B), bp, brows,
+                                static_cast<int>(K), num_sms(), s) != cudaSuccess) {
+      cudaFree(bp);
+      return LATENTMOE_ERR_CUDA;
+    }
+    const uint64_t tiles_half = static_cast<uint64_t>(groups * N / 128 * (K / lmoe::kGBK));
+    CUtensorMap tok, w0, w1;
+    bool ok = make_token_map(&tok, A, M, K);
+    ok &= make_tile_map(&w0, bp, tiles_half);
+    if (mode == 2)
+      ok &= make_tile_map(&w1, bp + groups * N * K, tiles_half);
+    else
+      w1 = w0;
+    if (!ok) {
+      cudaFree(bp);
+      return LATENTMOE_ERR_CUDA;
+    }
+    lmoe::GroupedArgs ga;
+    memset(&ga, 0, sizeof(ga));
+    ga.num_groups = static_cast<int>(groups);
+    ga.seg_offsets = offsets;
+    ga.fblocks = mode == 2 ? static_cast<int>(N / 128) : ceil_div(N, 256);
+    ga.kb = static_cast<int>(K / lmoe::kGBK);
+    ga.w_group_rows = static_cast<int>(N);
+    ga.n_out = static_cast<int>(N);
+    ga.out = C;
+    ga.ldo = N;
+    ga.status = status;
+    cudaError_t e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain,
+                                              tok, w0, w1, ga, num_sms(), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(bp);
+    return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
+  }
   GemmMaps m;
   bool ok = make_map(&m.a, A, M, K, K, 128);
   if (mode == 2) {

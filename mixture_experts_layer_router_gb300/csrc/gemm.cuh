@@ -47,9 +47,13 @@ constexpr int kMaxGroups = 512;
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kBarrierBytes = 8 * (2 * kStages + 2 + 2 + 1);
+// Epilogue staging: per epilogue warp, 32 rows x 64 bytes of bf16 output with
+// a 16-byte pad per row (80-byte pitch keeps 16-byte accesses conflict-free).
+constexpr int kStagePitch = 80;
+constexpr int kStageWarpBytes = 32 * kStagePitch;
 constexpr int kGemmSmemBytes =
     1024 /* alignment slack */ + kStages * kStageBytes + kBarrierBytes + 16 +
-    2 * (kMaxGroups + 1) * 4;
+    2 * (kMaxGroups + 1) * 4 + 4 * kStageWarpBytes;
 
 struct GemmArgs {
   int grouped;             // 0: dense rows [0, M); 1: segments from seg_offsets
@@ -116,16 +120,49 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmArgs& a, const
   return c;
 }
 
-// All lanes of a warp wait together: lane 0 polls, the verdict is broadcast,
-// then the other lanes observe the completed phase themselves.
-__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag, unsigned* status) {
+// bf16 output of one 32-column chunk for the warp's 32 rows. Each lane packs
+// its own row into the warp's staging rows, then the warp writes 8 rows per
+// instruction with 4 lanes per row (64 contiguous bytes). Rows at or past
+// `rows_valid` (relative to the warp's first row) are not stored; with
+// kEpiScatter, row t goes to rows pos[t*k + j] of the output instead.
+template <int MODE>
+__device__ __forceinline__ void store_chunk_bf16_staged(const GemmArgs& a,
+                                                        const uint32_t (&v)[32], uint8_t* stage,
+                                                        long long warp_row0, int rows_valid,
+                                                        int col) {
   const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) ok = wait_bounded(bar, parity, abort_flag, status) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && lane != 0) ok = mbar_try_wait(bar, parity) ? 1 : wait_bounded(bar, parity, abort_flag, status);
-  return __all_sync(0xffffffffu, ok) != 0;
+  uint4* mine = reinterpret_cast<uint4*>(stage + lane * kStagePitch);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+    w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+    w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+    w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+    mine[q] = w;
+  }
+  __syncwarp();
+  const int piece = lane & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rr = q * 8 + (lane >> 2);
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * kStagePitch + piece * 16);
+    if (rr < rows_valid) {
+      const long long row = warp_row0 + rr;
+      if constexpr (MODE == kEpiScatter) {
+        for (int j = 0; j < a.topk; ++j) {
+          const int dst_row = a.pos[row * a.topk + j];
+          if (dst_row < 0) continue;
+          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                    static_cast<long long>(dst_row) * a.ldo + col + piece * 8) = w;
+        }
+      } else {
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * a.ldo + col +
+                                  piece * 8) = w;
+      }
+    }
+  }
+  __syncwarp();
 }
 
 template <int MODE>
@@ -200,6 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
   int* mt_s = seg_s + kMaxGroups + 1;
+  uint8_t* stage_smem = reinterpret_cast<uint8_t*>(mt_s + kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -359,6 +397,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    uint8_t* stage_w = stage_smem + (warp - 2) * kStageWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
@@ -369,6 +408,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       const bool row_ok = r < c.rows;
       const long long row = static_cast<long long>(c.row0) + r;
+      const long long warp_row0 = static_cast<long long>(c.row0) + quarter * 32;
+      const int warp_rows = c.rows - quarter * 32;
       if constexpr (MODE == kEpiSwiglu) {
 #pragma unroll 1
         for (int ch = 0; ch < kBN / 64; ++ch) {
@@ -377,11 +418,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_32cols(tbase + kBN / 2 + ch * 32, u);
           tmem_ld_wait();
           const int col = c.n * (kBN / 2) + ch * 32;
-          if (row_ok && col < a.N) {
+          if (col < a.N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               g[i] = __float_as_uint(silu(__uint_as_float(g[i])) * __uint_as_float(u[i]));
-            store_chunk<kEpiBf16>(a, g, row, col);
+            store_chunk_bf16_staged<kEpiBf16>(a, g, stage_w, warp_row0, warp_rows, col);
           }
         }
       } else {
@@ -391,7 +432,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_32cols(tbase + ch * 32, v);
           tmem_ld_wait();
           const int col = c.n * kBN + ch * 32;
-          if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
+          if constexpr (MODE == kEpiF32) {
+            if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
+          } else {
+            if (col < a.N) store_chunk_bf16_staged<MODE>(a, v, stage_w, warp_row0, warp_rows, col);
+          }
         }
       }
       tc_fence_before_sync();

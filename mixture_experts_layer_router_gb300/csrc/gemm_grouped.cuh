@@ -1,0 +1,386 @@
+// Grouped tcgen05 GEMM for the expert FFNs, weights on the M side.
+//
+// For each expert e with n_e slots, the product is computed transposed:
+// D[feature, token] = W[feature, :] . Z[token, :], with M = 128 weight rows
+// and N = the expert's tokens (a multiple of 16, at most 256 per tile). Token
+// counts are only padded to 16, not to a 128-row tile, and one weight tile is
+// read once for all tokens of an expert (n_e <= 256) or for each 256-token
+// chunk (more tokens).
+//
+// Weights are read from the packed layout made by pack_weight_tiles: every
+// 128-row x 64-column tile is one contiguous 16 KB block, so the weight
+// stream reaches HBM as sequential reads instead of 128-byte pieces of rows
+// 6-20 KB apart.
+//
+// Each tile uses two accumulators that share one token tile in shared
+// memory: (gate, up) rows of the same 128 features for the SwiGLU GEMM, or
+// two consecutive 128-row blocks of W_d for the down GEMM. Together they
+// fill TMEM (2 x 256 columns), and a k-block moves 64 KB of shared memory for
+// 2 x 128 x 256 x 64 MACs.
+//
+//   warp 0      TMA producer (one lane): two packed weight tiles, then the
+//               token rows in 64-row boxes
+//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warps 2..9  epilogue: warp w reads TMEM lanes [32*(w%4), +32) and every
+//               other 32-token chunk; rows are transposed through shared
+//               memory so each output row segment is one 64-byte store
+//
+// Accumulators are single-buffered: the MMA of the next tile waits for the
+// epilogue, but the producer keeps filling the stage ring meanwhile, so the
+// memory system stays busy; the kernel is bound by the weight stream.
+//
+// Tiles are enumerated on the device from the segment offsets: expert-major,
+// then feature block, then token chunk, so chunks of one feature block run
+// on neighbouring CTAs at the same time and share the weight tile in L2.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace lmoe {
+
+enum GroupedMode : int { kGrpSwiglu = 0, kGrpPlain = 1 };
+
+constexpr int kGBK = 64;                      // one 128-byte swizzle row
+constexpr int kGStages = 3;
+constexpr int kGWeightTile = 128 * kGBK * 2;  // 16 KB
+constexpr int kGTokenTile = 256 * kGBK * 2;   // 32 KB
+constexpr int kGStageBytes = 2 * kGWeightTile + kGTokenTile;
+constexpr int kGTokBox = 64;                  // token rows per TMA box
+constexpr int kGTokBoxBytes = kGTokBox * kGBK * 2;
+constexpr int kGMaxTok = 256;
+constexpr int kGEpiWarps = 8;
+constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGBarrierBytes = 8 * (2 * kGStages + 3);
+constexpr int kGStagePitch = 80;              // 64 B of bf16 + 16 B pad per token row
+constexpr int kGStageWarpBytes = 32 * kGStagePitch;
+constexpr int kGMaxGroups = 512;
+constexpr int kGSmemBytes = 1024 + kGStages * kGStageBytes + kGBarrierBytes + 16 +
+                            2 * (kGMaxGroups + 1) * 4 + kGEpiWarps * kGStageWarpBytes;
+
+struct GroupedArgs {
+  int num_groups;          // G <= kGMaxGroups
+  const int* seg_offsets;  // [G+1] token row offsets of the groups
+  int fblocks;             // feature blocks per group (SwiGLU: F/128; plain: ceil(N/256))
+  int kb;                  // k-blocks (K / 64)
+  int w_group_rows;        // weight rows per group in the weight maps
+  int n_out;               // output features (columns of out)
+  void* out;               // bf16 [rows, n_out], rows in slot order
+  long long ldo;
+  unsigned* status;
+};
+
+struct GTile {
+  int tok0;   // first token row
+  int len;    // valid tokens (<= 256)
+  int n;      // MMA N: len rounded up to 16
+  int f;      // feature block
+  int wrow;   // first weight row of accumulator 0
+};
+
+__device__ __forceinline__ void group_chunks(int n, int& nch, int& cs) {
+  nch = (n + kGMaxTok - 1) / kGMaxTok;
+  const int per = (n + nch - 1) / nch;
+  cs = (per + 15) & ~15;
+}
+
+template <int MODE>
+__device__ __forceinline__ GTile decode_gtile(int t, const GroupedArgs& a, const int* seg_s,
+                                              const int* tp_s) {
+  int lo = 0, hi = a.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tp_s[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int n = seg_s[g + 1] - seg_s[g];
+  int nch, cs;
+  group_chunks(n, nch, cs);
+  const int local = t - tp_s[g];
+  const int f = local / nch;
+  const int c = local - f * nch;
+  GTile r;
+  r.tok0 = seg_s[g] + c * cs;
+  r.len = min(cs, n - c * cs);
+  r.n = (r.len + 15) & ~15;
+  r.f = f;
+  r.wrow = g * a.w_group_rows + f * (MODE == kGrpSwiglu ? 128 : 256);
+  return r;
+}
+
+template <int MODE>
+__device__ __forceinline__ bool second_acc_used(const GroupedArgs& a, int f) {
+  return MODE == kGrpSwiglu || (f * 256 + 128 < a.n_out);
+}
+
+// Transpose one 32-token x 32-feature chunk (p: this lane's feature for 32
+// tokens, bf16 pairs (token 2j, 2j+1) in p[j]) through the warp's staging rows
+// and store 64 contiguous bytes per token row. Tokens at or past `tok_valid`
+// are not stored.
+__device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_t (&p)[16],
+                                             uint8_t* stage, long long tok_row0, int tok_valid,
+                                             int feat0) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    *reinterpret_cast<uint16_t*>(stage + (2 * j) * kGStagePitch + lane * 2) =
+        static_cast<uint16_t>(p[j] & 0xffffu);
+    *reinterpret_cast<uint16_t*>(stage + (2 * j + 1) * kGStagePitch + lane * 2) =
+        static_cast<uint16_t>(p[j] >> 16);
+  }
+  __syncwarp();
+  const int piece = lane & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rr = q * 8 + (lane >> 2);
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * kGStagePitch + piece * 16);
+    if (rr < tok_valid)
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                (tok_row0 + rr) * a.ldo + feat0 + piece * 8) = w;
+  }
+  __syncwarp();
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_grouped_kernel(const __grid_constant__ CUtensorMap tmTok,
+                        const __grid_constant__ CUtensorMap tmW0,
+                        const __grid_constant__ CUtensorMap tmW1, const GroupedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kGStages * kGStageBytes);
+  uint64_t* empty_bar = full_bar + kGStages;
+  uint64_t* tfull_bar = empty_bar + kGStages;
+  uint64_t* tempty_bar = tfull_bar + 1;
+  uint64_t* done_bar = tempty_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
+  int* tp_s = seg_s + kGMaxGroups + 1;
+  uint8_t* stage_smem = reinterpret_cast<uint8_t*>(tp_s + kGMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 32 * kGEpiWarps);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmTok);
+    tma_prefetch_desc(&tmW0);
+    tma_prefetch_desc(&tmW1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
+  __syncthreads();
+  if (warp == 2) {
+    // exclusive prefix over groups of (token chunks x feature blocks)
+    int carry = 0;
+    if (lane == 0) tp_s[0] = 0;
+    for (int base = 0; base < a.num_groups; base += 32) {
+      const int g = base + lane;
+      int v = 0;
+      if (g < a.num_groups) {
+        const int n = seg_s[g + 1] - seg_s[g];
+        if (n > 0) {
+          int nch, cs;
+          group_chunks(n, nch, cs);
+          v = nch * a.fblocks;
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (g < a.num_groups) tp_s[g + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tp_s[a.num_groups];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      // Weights come from the packed layout: tile (row tile rt, k-block kb)
+      // is one contiguous 16 KB block at index rt * kb_count + kb.
+      const uint64_t pol_w = policy_evict_normal();
+      const uint64_t pol_t = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+        const bool two = second_acc_used<MODE>(a, c.f);
+        const int nbox = (c.n + kGTokBox - 1) / kGTokBox;
+        const uint32_t bytes = kGWeightTile * (two ? 2 : 1) + nbox * kGTokBoxBytes;
+        const int rt0 = c.wrow / 128;
+        for (int kb = 0; kb < a.kb; ++kb) {
+          if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw0 = tiles + stage * kGStageBytes;
+          uint8_t* sw1 = sw0 + kGWeightTile;
+          uint8_t* stok = sw1 + kGWeightTile;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          tma_load_3d(&tmW0, &full_bar[stage], sw0, 0, 0, rt0 * a.kb + kb, pol_w);
+          if (two) {
+            if (MODE == kGrpSwiglu)
+              tma_load_3d(&tmW1, &full_bar[stage], sw1, 0, 0, rt0 * a.kb + kb, pol_w);
+            else
+              tma_load_3d(&tmW0, &full_bar[stage], sw1, 0, 0, (rt0 + 1) * a.kb + kb, pol_w);
+          }
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(&tmTok, &full_bar[stage], stok + b * kGTokBoxBytes, kb * kGBK,
+                        c.tok0 + b * kGTokBox, pol_t);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < kGStages; ++s)
+        if (issued_mask & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+        const bool two = second_acc_used<MODE>(a, c.f);
+        const uint32_t idesc = instr_desc_bf16(128, c.n);
+        if (!wait_bounded(tempty_bar, acc_phase ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after_sync();
+        for (int kb = 0; kb < a.kb; ++kb) {
+          if (!wait_bounded(&full_bar[stage], phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint8_t* sw0 = tiles + stage * kGStageBytes;
+          const uint64_t d0 = smem_desc_sw128(sw0);
+          const uint64_t d1 = smem_desc_sw128(sw0 + kGWeightTile);
+          const uint64_t dt = smem_desc_sw128(sw0 + 2 * kGWeightTile);
+#pragma unroll
+          for (int k = 0; k < kGBK / 16; ++k) {
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            tc_mma(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+            if (two) tc_mma(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar);
+        acc_phase ^= 1u;
+      }
+      tc_commit(done_bar);
+      wait_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* stage_w = stage_smem + (warp - 2) * kGStageWarpBytes;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+      const bool two = second_acc_used<MODE>(a, c.f);
+      if (!warp_wait_bounded(tfull_bar, acc_phase, abort_flag, a.status)) break;
+      tc_fence_after_sync();
+      const int nchunks = (c.len + 31) / 32;
+      if constexpr (MODE == kGrpSwiglu) {
+        // Read both accumulators and form h = SiLU(gate) * up for this
+        // warp's chunks (at most 4), packed to bf16 in registers; then hand
+        // TMEM back to the MMA before the slower transposing stores.
+        uint32_t hp[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = half + 2 * i;
+          if (ch < nchunks) {
+            uint32_t g[32], u[32];
+            tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
+            tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              hp[i][j] = pack_bf16x2(silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]),
+                                     silu(__uint_as_float(g[2 * j + 1])) *
+                                         __uint_as_float(u[2 * j + 1]));
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(tempty_bar);
+        const int feat0 = c.f * 128 + quarter * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = half + 2 * i;
+          if (ch < nchunks)
+            gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+                         c.len - ch * 32, feat0);
+        }
+      } else {
+        for (int ch = half; ch < nchunks; ch += 2) {
+          const long long tok_row0 = static_cast<long long>(c.tok0) + ch * 32;
+          const int tok_valid = c.len - ch * 32;
+#pragma unroll 1
+          for (int acc = 0; acc < 2; ++acc) {
+            if (acc == 1 && !two) break;
+            uint32_t v[32];
+            tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
+            tmem_ld_wait();
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            const int feat0 = c.f * 256 + acc * 128 + quarter * 32;
+            if (feat0 < a.n_out) gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(tempty_bar);
+      }
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace lmoe

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm.cuh"
+#include "gemm_grouped.cuh"
 
 namespace lmoe {
 
@@ -20,6 +21,17 @@ cudaError_t launch_gemm_f32(const GemmMaps& m, const GemmArgs& a, int grid, bool
                             cudaStream_t s);
 cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+
+// One launch of gemm_grouped_kernel<mode> (kGrpSwiglu or kGrpPlain):
+// tok = token rows (64-row boxes), w0/w1 = weight rows (128-row boxes).
+cudaError_t launch_gemm_grouped(int mode, const CUtensorMap& tok, const CUtensorMap& w0,
+                                const CUtensorMap& w1, const GroupedArgs& a, int grid,
+                                cudaStream_t s);
+
+// Rewrite W [rows, K] (rows % 128 == 0, K % kGBK == 0) as contiguous
+// 128 x kGBK tiles, tile index (row / 128) * (K / kGBK) + k / kGBK.
+cudaError_t launch_pack_tiles(const __nv_bfloat16* src, __nv_bfloat16* dst, long long rows, int K,
+                              int sms, cudaStream_t s);
 
 // Softmax over E and stable top-k per token: idx [T,k] int32, gates [T,k].
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,

@@ -86,6 +86,18 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
   }
 }
 
+// All lanes of a warp wait together: lane 0 polls, the verdict is broadcast,
+// then the other lanes observe the completed phase themselves.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = wait_bounded(bar, parity, abort_flag, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok && lane != 0) ok = mbar_try_wait(bar, parity) ? 1 : wait_bounded(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // Teardown variant: no abort check (used to drain copies already in flight).
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -108,6 +120,17 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+// 3-D tiled load of the box at (c0, c1, c2) (c0 innermost).
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "l"(policy)
       : "memory");
 }
 
@@ -204,6 +227,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* tile) {
          (2ull << 61);
 }
 
+// Same for a K-major bf16 tile written by TMA with 64-byte swizzle: rows of
+// 64 bytes (32 elements), 8-row groups 512 bytes apart; layout type 4.
+__device__ __forceinline__ uint64_t smem_desc_sw64(const void* tile) {
+  const uint64_t addr = smem_addr(tile);
+  return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | (32ull << 32) | (1ull << 46) |
+         (4ull << 61);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits [4,6) = 1),
 // A and B bf16 (bits [7,10) and [10,13) = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits [17,23), M >> 4 in bits [24,29).
@@ -218,6 +249,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + __expf(-a)); }
+// SiLU(a) = a / (1 + e^-a) with the hardware exponential and reciprocal
+// (about 2^-21 relative error; the result is rounded to bf16 afterwards).
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 }  // namespace lmoe

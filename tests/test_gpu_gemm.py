@@ -61,11 +61,17 @@ def test_dense_swiglu(M, N, K):
     _check(C, g / (1 + torch.exp(-g)) * u)
 
 
-@pytest.mark.parametrize("mode", [0, 2])
-def test_grouped(mode):
+@pytest.mark.parametrize("mode,N,offsets", [
+    (0, 256, [0, 0, 130, 130, 400, 700, 701]),
+    (2, 256, [0, 0, 130, 130, 400, 700, 701]),
+    (0, 128, [0, 1, 18, 618, 874, 875]),          # second accumulator unused
+    (0, 384, [0, 255, 256, 513, 1200]),           # chunked groups, half-used block
+    (2, 128, [0, 17, 17, 300, 1100, 1101, 1357]),
+    (2, 384, [0, 64, 64, 64, 320]),
+])
+def test_grouped(mode, N, offsets):
     gh.lib()
-    offsets = [0, 0, 130, 130, 400, 700, 701]
-    G, M, N, K = len(offsets) - 1, offsets[-1], 256, 256
+    G, M, K = len(offsets) - 1, offsets[-1], 256
     A = _rand((M, K), 7)
     Bn = N * G * (2 if mode == 2 else 1)
     B = _rand((Bn, K), 8, 0.1)
