@@ -83,6 +83,17 @@ def profiled_traffic(workload: str):
     return float(m_tr.group(1)) if m_sha.group(1) == cur else None
 
 
+def max_over_ranks(value: float, dist, device="cpu") -> float:
+    """The largest value over all ranks (the job's time is its slowest rank's);
+    the value itself on one process."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -305,10 +316,7 @@ def run_ours(args, cfg, rank, world, dist):
     status = layer.status()
     layer.set_profiling(0)
 
-    if dist is not None:
-        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, "cuda")
 
     # end to end through the host-buffer entry point: pinned x in, y out
     e2e = None
@@ -323,11 +331,7 @@ def run_ours(args, cfg, rank, world, dist):
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             layer.forward_host(xh, yh)
-        dt = time.perf_counter() - t0
-        if dist is not None:
-            tt = torch.tensor([dt], dtype=torch.float64, device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            dt = float(tt.item())
+        dt = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
         e2e = {"value": world * cfg.T * n_e2e / dt, "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                "steps": n_e2e}
