@@ -125,6 +125,21 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w);
 int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T,
                       latentmoe_stream_t stream);
 
+/* Router replay: the forward with the expert choices given instead of
+ * selected ("The Training and RL Infrastructure Behind MAI-Thinking-1":
+ * the MoE layer supports router replay, section "Sharding and parallelism";
+ * choices recorded at inference are replayed in the learner's pass, section
+ * "4. RL infrastructure"). idx: device int32 [T, k], expert ids of each
+ * token in slot order j. gates: device fp32 [T, k], or NULL to use the
+ * softmax probabilities of the replayed experts under this layer's router
+ * (divided by their sum with LATENTMOE_RENORM). With gates given, the router
+ * GEMM is not run. Ids outside [0, E) are dropped from the combine (that slot
+ * contributes nothing) and set LATENTMOE_STATUS_BAD_EXPERT. Otherwise as
+ * latentmoe_forward. */
+int latentmoe_forward_routed(latentmoe_t h, const void* x, const int32_t* idx,
+                             const float* gates, void* out, int64_t T,
+                             latentmoe_stream_t stream);
+
 /* The same forward with HOST buffers: copies x_host (bf16 [T, d]) to the
  * device, runs latentmoe_forward, copies the result to out_host, and
  * synchronises `stream` before returning. Page-locked host memory gives

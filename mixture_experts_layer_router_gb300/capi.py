@@ -50,6 +50,8 @@ SIGNATURES = {
                                         ctypes.c_uint32, ctypes.POINTER(_c_void_p)]),
     "latentmoe_load_weights": (ctypes.c_int, [_c_void_p, ctypes.POINTER(latentmoe_weights)]),
     "latentmoe_forward": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
+    "latentmoe_forward_routed": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                                _c_void_p, _i64, _c_void_p]),
     "latentmoe_forward_host": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "latentmoe_destroy": (ctypes.c_int, [_c_void_p]),
     "latentmoe_route_from_logits": (ctypes.c_int, [_c_void_p, _c_void_p, _i64] + [_c_void_p] * 7),
@@ -161,6 +163,18 @@ class LatentMoE:
             out = torch.empty((T, self.dims.hidden), dtype=dt, device=x.device)
         check(load().latentmoe_forward(self.handle, x.data_ptr(), out.data_ptr(), T,
                                        _stream(stream)), "latentmoe_forward")
+        return out
+
+    def forward_routed(self, x, idx, gates=None, out=None, stream=None):
+        """Router replay: idx [T, k] int32 (and optionally gates [T, k] fp32) given."""
+        import torch
+        T = x.shape[0]
+        if out is None:
+            dt = torch.float32 if self.flags & OUT_FP32 else torch.bfloat16
+            out = torch.empty((T, self.dims.hidden), dtype=dt, device=x.device)
+        check(load().latentmoe_forward_routed(self.handle, x.data_ptr(), idx.data_ptr(),
+                                              _ptr(gates), out.data_ptr(), T, _stream(stream)),
+              "latentmoe_forward_routed")
         return out
 
     def forward_host(self, x_host, out_host, stream=None):

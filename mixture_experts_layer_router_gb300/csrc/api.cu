@@ -182,18 +182,25 @@ void record(latentmoe* h, int slot_base, int i, cudaStream_t s) {
   if (h->prof_slots > 0) cudaEventRecord(h->events[slot_base + i], s);
 }
 
+// Counting sort of the workspace idx into counts, offsets, perm, pos.
+int run_sort(latentmoe* h, int T, cudaStream_t s) {
+  const int E = static_cast<int>(h->dims.num_experts);
+  LMOE_CK(h, lmoe::launch_sort(h->idx, T * h->k, h->k, E, h->cnt, h->cbase, h->counts,
+                               h->offsets, h->perm, h->pos, h->status, s));
+  h->launches += lmoe::kSortLaunches;
+  return LATENTMOE_OK;
+}
+
 // Routing half shared by forward and route_from_logits: logits -> idx,
 // gates -> counts, offsets, perm, pos (workspace buffers).
 int run_routing(latentmoe* h, const float* logits, int T, cudaStream_t s, int slot_base) {
   const int E = static_cast<int>(h->dims.num_experts);
-  const int S = T * h->k;
   LMOE_CK(h, lmoe::launch_route_topk(logits, T, E, h->k, (h->flags & LATENTMOE_RENORM) ? 1 : 0,
                                      h->idx, h->gates, s));
   h->launches += 1;
   record(h, slot_base, 2, s);
-  LMOE_CK(h, lmoe::launch_sort(h->idx, S, h->k, E, h->cnt, h->cbase, h->counts, h->offsets,
-                               h->perm, h->pos, h->status, s));
-  h->launches += lmoe::kSortLaunches;
+  const int r = run_sort(h, T, s);
+  if (r != LATENTMOE_OK) return r;
   record(h, slot_base, 3, s);
   return LATENTMOE_OK;
 }
@@ -426,12 +433,12 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   return LATENTMOE_OK;
 }
 
-int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latentmoe_stream_t st) {
-  if (h == nullptr || x == nullptr || out == nullptr) return LATENTMOE_ERR_INVALID_ARG;
-  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
-  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
-  if (!aligned16(x) || !aligned16(out)) return LATENTMOE_ERR_UNSUPPORTED;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+namespace {
+
+// The forward. With replay_idx the expert choices are the caller's (router
+// replay); with replay_gates as well the router is not run at all.
+int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_t s,
+                 const int32_t* replay_idx, const float* replay_gates) {
   LMOE_CK(h, cudaSetDevice(h->device));
   const latentmoe_dims& d = h->dims;
   const int E = static_cast<int>(d.num_experts), k = h->k;
@@ -467,14 +474,31 @@ int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latent
     a.out = h->logits;
     a.ldo = E;
     a.bias = (h->flags & LATENTMOE_ROUTER_BIAS) ? h->w.b_r : nullptr;
-    LMOE_CK(h, lmoe::launch_gemm_f32(m, a, dense_grid(h, Ti, a.n_tiles), false, s));
-    h->launches += 1;
+    if (replay_gates == nullptr) {
+      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, dense_grid(h, Ti, a.n_tiles), false, s));
+      h->launches += 1;
+    }
   }
   record(h, slot_base, 1, s);
-  // 1-2: softmax + top-k, counting sort
-  {
+  // 1-2: softmax + top-k (or the replayed choices), counting sort
+  if (replay_idx == nullptr) {
     const int r = run_routing(h, h->logits, Ti, s, slot_base);
     if (r != LATENTMOE_OK) return r;
+  } else {
+    LMOE_CK(h, cudaMemcpyAsync(h->idx, replay_idx, static_cast<size_t>(S) * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    if (replay_gates != nullptr) {
+      LMOE_CK(h, cudaMemcpyAsync(h->gates, replay_gates, static_cast<size_t>(S) * 4,
+                                 cudaMemcpyDeviceToDevice, s));
+    } else {
+      LMOE_CK(h, lmoe::launch_replay_gates(h->logits, Ti, E, h->idx, k,
+                                           (h->flags & LATENTMOE_RENORM) ? 1 : 0, h->gates, s));
+      h->launches += 1;
+    }
+    record(h, slot_base, 2, s);
+    const int r = run_sort(h, Ti, s);
+    if (r != LATENTMOE_OK) return r;
+    record(h, slot_base, 3, s);
   }
   // 3: latent down-projection scattered to the expert-sorted slots
   {
@@ -569,6 +593,32 @@ int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latent
   record(h, slot_base, 9, s);
   h->last_T = T;
   return LATENTMOE_OK;
+}
+
+int check_forward_args(latentmoe_t h, const void* x, void* out, int64_t T) {
+  if (h == nullptr || x == nullptr || out == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
+  if (!aligned16(x) || !aligned16(out)) return LATENTMOE_ERR_UNSUPPORTED;
+  return LATENTMOE_OK;
+}
+
+}  // namespace
+
+int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T, latentmoe_stream_t st) {
+  const int r = check_forward_args(h, x, out, T);
+  if (r != LATENTMOE_OK) return r;
+  return forward_impl(h, x, out, T, reinterpret_cast<cudaStream_t>(st), nullptr, nullptr);
+}
+
+int latentmoe_forward_routed(latentmoe_t h, const void* x, const int32_t* idx,
+                             const float* gates, void* out, int64_t T, latentmoe_stream_t st) {
+  const int r = check_forward_args(h, x, out, T);
+  if (r != LATENTMOE_OK) return r;
+  if (idx == nullptr || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(gates) & 3u))
+    return LATENTMOE_ERR_INVALID_ARG;
+  return forward_impl(h, x, out, T, reinterpret_cast<cudaStream_t>(st), idx, gates);
 }
 
 int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host, int64_t T,

@@ -37,6 +37,11 @@ cudaError_t launch_pack_tiles(const __nv_bfloat16* src, __nv_bfloat16* dst, long
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
                               float* gates, cudaStream_t s);
 
+// Router replay: gates[t,j] = softmax(logits[t])[idx[t,j]] (0 for ids outside
+// [0, E)), divided by their sum with renorm.
+cudaError_t launch_replay_gates(const float* logits, int T, int E, const int* idx, int k,
+                                int renorm, float* gates, cudaStream_t s);
+
 // Counting sort of the T*k slots by expert. Scratch: cnt and cbase, each
 // sort_scratch_ints(S, E) ints. Three launches.
 constexpr int kSortChunk = 1024;

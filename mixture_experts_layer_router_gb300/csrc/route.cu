@@ -95,6 +95,76 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+// Router replay without gates: the softmax probabilities (over all E, same
+// reductions as route_topk_kernel) of given expert choices. Ids outside
+// [0, E) get gate 0 (the counting sort drops them and flags the status).
+template <int VPL>
+__global__ void __launch_bounds__(256) replay_gates_kernel(const float* __restrict__ logits, int T,
+                                                           int E, const int* __restrict__ idx,
+                                                           int k, int renorm,
+                                                           float* __restrict__ gates) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + static_cast<long long>(t) * E;
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    float x = (e < E) ? row[e] : -INFINITY;
+    v[i] = (x != x) ? -INFINITY : x;
+  }
+  float m = v[0];
+#pragma unroll
+  for (int i = 1; i < VPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) {
+    float g[16];
+    float gsum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      g[j] = 0.0f;
+      if (j < k) {
+        const int e = idx[static_cast<long long>(t) * k + j];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+          float x = row[e];
+          x = (x != x) ? -INFINITY : x;
+          g[j] = expf(x - m) / s;
+        }
+        gsum += g[j];
+      }
+    }
+    const float scale = (renorm && gsum > 0.0f) ? 1.0f / gsum : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < k) gates[static_cast<long long>(t) * k + j] = renorm ? g[j] * scale : g[j];
+  }
+}
+
+cudaError_t launch_replay_gates(const float* logits, int T, int E, const int* idx, int k,
+                                int renorm, float* gates, cudaStream_t s) {
+  const int blocks = (T + 7) / 8;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    replay_gates_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, idx, k, renorm, gates);
+  else if (vpl <= 2)
+    replay_gates_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, idx, k, renorm, gates);
+  else if (vpl <= 4)
+    replay_gates_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, idx, k, renorm, gates);
+  else if (vpl <= 8)
+    replay_gates_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, idx, k, renorm, gates);
+  else
+    replay_gates_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, idx, k, renorm, gates);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
                               float* gates, cudaStream_t s) {
   const int blocks = (T + 7) / 8;

@@ -57,8 +57,11 @@ def _pick_top_k(L: List[float], k: int) -> List[int]:
 
 def forward(x, w_r, w_dn, w_up, w_g, w_u, w_d, k: int, b_r=None,
             renorm: bool = False, w_gs=None, w_us=None, w_ds=None,
-            logits=None) -> Dict[str, object]:
-    """All arguments are nested lists (or arrays indexable as lists)."""
+            logits=None, replay_idx=None, replay_gates=None) -> Dict[str, object]:
+    """All arguments are nested lists (or arrays indexable as lists).
+
+    ``replay_idx`` [T][k] replaces the top-k choice (router replay); with
+    ``replay_gates`` the gates are taken as given as well."""
     T = len(x)
     E = len(w_r)
     idx_all, gates_all, y_all, L_all = [], [], [], []
@@ -76,9 +79,11 @@ def forward(x, w_r, w_dn, w_up, w_g, w_u, w_d, k: int, b_r=None,
         for v in ex:
             tot += v
         p = [v / tot for v in ex]
-        idx = _pick_top_k(L, k)
+        idx = _pick_top_k(L, k) if replay_idx is None else [int(e) for e in replay_idx[t]]
         gates = [p[e] for e in idx]
-        if renorm:
+        if replay_gates is not None:
+            gates = [float(g) for g in replay_gates[t]]
+        elif renorm:
             gs = sum(gates)
             gates = [g / gs for g in gates]
         # dense over all experts: weight 0 unless selected

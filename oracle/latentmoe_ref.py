@@ -221,6 +221,39 @@ def forward(x: np.ndarray, weights: OracleWeights, k: int, renorm: bool = False,
             "H": H, "c": c, "y": y}
 
 
+def forward_routed(x: np.ndarray, weights: OracleWeights, idx: np.ndarray,
+                   gates: Optional[np.ndarray] = None, renorm: bool = False,
+                   logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The layer with the expert choices given (router replay).
+
+    "The Training and RL Infrastructure Behind MAI-Thinking-1": the MoE layer
+    supports router replay (section "Sharding and parallelism"), and the
+    expert choices made during inference are recorded and replayed in the
+    learner's pass (section "4. RL infrastructure"). ``idx`` [T, k] replaces
+    steps 1-3. Gates are taken as given; when ``gates`` is None they are the
+    softmax probabilities of the replayed experts under this layer's router
+    (step 4 on the replayed choices).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    E = weights.num_experts
+    if gates is None:
+        L = router_logits(x, weights.w_r, weights.b_r) if logits is None else \
+            np.asarray(logits, dtype=np.float64)
+        g = select_gates(softmax_rows(L), idx, renorm)
+    else:
+        g = np.asarray(gates, dtype=np.float64)
+    z = latent_down(x, weights.w_dn)
+    counts, offsets, perm, pos = counting_sort(idx, E)
+    H = run_experts(z, perm, offsets, weights)
+    c = combine(H, g, pos)
+    y = latent_up(c, weights.w_up)
+    if weights.w_gs is not None:
+        y = y + shared_expert(x, weights.w_gs, weights.w_us, weights.w_ds)
+    return {"idx": idx, "gates": g, "counts": counts, "offsets": offsets, "perm": perm,
+            "pos": pos, "c": c, "y": y}
+
+
 def route(logits: np.ndarray, E: int, k: int, renorm: bool = False) -> Dict[str, np.ndarray]:
     """Steps 2-4 and 6 from given logits: the routing half of the layer."""
     L = np.asarray(logits, dtype=np.float64)

@@ -313,8 +313,37 @@ def check_shared_only(ref):
     np.testing.assert_allclose(out["y"], s, rtol=1e-13, atol=1e-13)
 
 
+def check_replay(ref):
+    """Router replay: the layer's own choices reproduce forward(); foreign
+    choices and gates match brute force with the same replayed routing."""
+    from oracle import latentmoe_brute as brute
+    for c in (dict(seed=61, bias=True), dict(seed=62, Fs=2, k=3, E=4)):
+        w = tiny_layer(**c)
+        W = oracle_weights(ref, w)
+        out = ref.forward(w["x"], W, w["k"])
+        rep = ref.forward_routed(w["x"], W, out["idx"])
+        np.testing.assert_allclose(rep["y"], out["y"], rtol=0, atol=1e-14)
+        rng = np.random.default_rng(c["seed"])
+        T, E, k = w["x"].shape[0], w["w_r"].shape[0], w["k"]
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        for gates in (None, rng.uniform(0.1, 1.0, (T, k))):
+            got = ref.forward_routed(w["x"], W, idx, gates)
+            bf = brute.forward(w["x"].tolist(), w["w_r"].tolist(), w["w_dn"].tolist(),
+                               w["w_up"].tolist(), w["w_g"].tolist(), w["w_u"].tolist(),
+                               w["w_d"].tolist(), k,
+                               b_r=None if w["b_r"] is None else w["b_r"].tolist(),
+                               w_gs=None if w["w_gs"] is None else w["w_gs"].tolist(),
+                               w_us=None if w["w_us"] is None else w["w_us"].tolist(),
+                               w_ds=None if w["w_ds"] is None else w["w_ds"].tolist(),
+                               replay_idx=idx.tolist(),
+                               replay_gates=None if gates is None else gates.tolist())
+            np.testing.assert_allclose(got["y"], np.array(bf["y"]), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(got["gates"], np.array(bf["gates"]), rtol=0, atol=1e-12)
+            assert np.array_equal(got["pos"], np.array(bf["pos"]))
+
+
 ALL_CHECKS = [
     check_brute_force, check_closed_forms, check_tie_break, check_dense_sandwich,
     check_full_mixture, check_gates, check_counting_sort, check_zero_input,
-    check_token_permutation, check_expert_permutation, check_shared_only,
+    check_token_permutation, check_expert_permutation, check_shared_only, check_replay,
 ]
