@@ -7,8 +7,9 @@
 // host synchronisation (token counts per expert stay on the device, as in
 // "Frontier Pre-training at Microsoft AI", section "Reducing per-expert
 // overhead"):
-//   0 router_gemm     logits = x W_r^T (+ b)                 tcgen05, fp32 out
-//   1 route_topk      softmax + stable top-k                 warp per token
+//   0 router          logits = x W_r^T (+ b), softmax, stable tcgen05, fused
+//                     top-k, gates                           epilogue
+//   1 replay_gates    (router replay without gates only)
 //   2 sort            counts, offsets, perm, pos             3 small kernels
 //   3 down_proj       z = x W_dn^T, written to the k slots   tcgen05, scatter
 //   4 expert_gate_up  h = SiLU(z W_g^T) * (z W_u^T)          tcgen05, grouped
@@ -34,8 +35,8 @@ namespace {
 
 constexpr int kNumStages = 9;
 const char* const kStageNames[kNumStages] = {
-    "router_gemm", "route_topk", "sort",   "down_proj", "expert_gate_up",
-    "expert_down", "combine",    "shared_gate_up", "up_proj"};
+    "router",      "replay_gates", "sort",           "down_proj", "expert_gate_up",
+    "expert_down", "combine",      "shared_gate_up", "up_proj"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -121,6 +122,7 @@ struct latentmoe {
   void* wmem = nullptr;          // one allocation holding every weight copy
   GemmMaps m_router, m_down, m_shared, m_up;
   CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
+  CUtensorMap m_wr32;            // router weights in 32-column boxes (router kernel)
   // workspace
   void* ws = nullptr;
   float* logits = nullptr;
@@ -408,6 +410,7 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
 
   bool ok = true;
   ok &= make_map(&h->m_router.b, o.w_r, E, dd, dd, 256);
+  ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);
   ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
   ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l / lmoe::kGBK));
   ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l / lmoe::kGBK));
@@ -448,8 +451,9 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   const bool out32 = (h->flags & LATENTMOE_OUT_FP32) != 0;
 
   // activation maps for this call
-  CUtensorMap mx, mzp, mh, mc, msh;
+  CUtensorMap mx, mx32, mzp, mh, mc, msh;
   bool ok = make_map(&mx, x, T, dd, dd, 128);
+  ok &= make_map(&mx32, x, T, dd, dd, 128, lmoe::kRBK);
   ok &= make_token_map(&mzp, h->zp, S, l);
   ok &= make_token_map(&mh, h->hb, S, F);
   ok &= make_map(&mc, h->cb, T, l, l, 128);
@@ -462,29 +466,27 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   h->forwards += 1;
   record(h, slot_base, 0, s);
 
-  // 0: router logits (fp32, + bias)
-  {
-    GemmMaps m = h->m_router;
-    m.a = mx;
-    GemmArgs a = base_args(h);
-    a.M = Ti;
-    a.N = E;
-    a.n_tiles = ceil_div(E, lmoe::kBN);
-    a.kb1 = dd / lmoe::kBK;
-    a.out = h->logits;
-    a.ldo = E;
-    a.bias = (h->flags & LATENTMOE_ROUTER_BIAS) ? h->w.b_r : nullptr;
-    if (replay_gates == nullptr) {
-      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, dense_grid(h, Ti, a.n_tiles), false, s));
-      h->launches += 1;
-    }
+  // 0: router GEMM + softmax + stable top-k (fused); skipped when the caller
+  // replays both choices and gates
+  if (replay_gates == nullptr) {
+    lmoe::RouterArgs ra;
+    memset(&ra, 0, sizeof(ra));
+    ra.T = Ti;
+    ra.E = E;
+    ra.k = k;
+    ra.renorm = (h->flags & LATENTMOE_RENORM) ? 1 : 0;
+    ra.kb = dd / lmoe::kRBK;
+    ra.bias = (h->flags & LATENTMOE_ROUTER_BIAS) ? h->w.b_r : nullptr;
+    ra.logits = h->logits;
+    ra.idx = h->idx;
+    ra.gates = h->gates;
+    ra.status = h->status;
+    LMOE_CK(h, lmoe::launch_router_topk(mx32, h->m_wr32, ra, h->sms, s));
+    h->launches += 1;
   }
   record(h, slot_base, 1, s);
-  // 1-2: softmax + top-k (or the replayed choices), counting sort
-  if (replay_idx == nullptr) {
-    const int r = run_routing(h, h->logits, Ti, s, slot_base);
-    if (r != LATENTMOE_OK) return r;
-  } else {
+  // 1: replayed choices (and gates from the router's softmax if not given)
+  if (replay_idx != nullptr) {
     LMOE_CK(h, cudaMemcpyAsync(h->idx, replay_idx, static_cast<size_t>(S) * 4,
                                cudaMemcpyDeviceToDevice, s));
     if (replay_gates != nullptr) {
@@ -495,11 +497,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
                                            (h->flags & LATENTMOE_RENORM) ? 1 : 0, h->gates, s));
       h->launches += 1;
     }
-    record(h, slot_base, 2, s);
+  }
+  record(h, slot_base, 2, s);
+  // 2: counting sort
+  {
     const int r = run_sort(h, Ti, s);
     if (r != LATENTMOE_OK) return r;
-    record(h, slot_base, 3, s);
   }
+  record(h, slot_base, 3, s);
   // 3: latent down-projection scattered to the expert-sorted slots
   {
     GemmMaps m = h->m_down;

@@ -7,6 +7,7 @@
 
 #include "gemm.cuh"
 #include "gemm_grouped.cuh"
+#include "router.cuh"
 
 namespace lmoe {
 
@@ -32,6 +33,11 @@ cudaError_t launch_gemm_grouped(int mode, const CUtensorMap& tok, const CUtensor
 // 128 x kGBK tiles, tile index (row / 128) * (K / kGBK) + k / kGBK.
 cudaError_t launch_pack_tiles(const __nv_bfloat16* src, __nv_bfloat16* dst, long long rows, int K,
                               int sms, cudaStream_t s);
+
+// Router GEMM fused with softmax and stable top-k: logits [T,E] fp32 (+bias),
+// idx [T,k], gates [T,k]; x map in 128-row boxes, W_r map in 256-row boxes.
+cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,
+                               cudaStream_t s);
 
 // Softmax over E and stable top-k per token: idx [T,k] int32, gates [T,k].
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,

@@ -1,0 +1,37 @@
+// Router GEMM + softmax + stable top-k (one fused kernel); see router.cuh.
+#include "kernels.h"
+#include "router.cuh"
+
+namespace lmoe {
+
+template <int KMAX>
+static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a,
+                                      int sms, cudaStream_t s) {
+  const int per_stage = router_stage_bytes(a.E);
+  const int fixed = router_fixed_smem<KMAX>();
+  a.stages = (kRMaxSmem - fixed) / per_stage;
+  if (a.stages > kRMaxStages) a.stages = kRMaxStages;
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  const int smem = fixed + a.stages * per_stage;
+  static bool smem_set = false;
+  if (!smem_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        router_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRMaxSmem);
+    if (e != cudaSuccess) return e;
+    smem_set = true;
+  }
+  const int m_tiles = (a.T + 127) / 128;
+  const int grid = m_tiles < sms ? m_tiles : sms;
+  router_topk_kernel<KMAX><<<grid, kRThreads, smem, s>>>(x, w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,
+                               cudaStream_t s) {
+  if (a.k <= 2) return launch_router_impl<2>(x, w, a, sms, s);
+  if (a.k <= 4) return launch_router_impl<4>(x, w, a, sms, s);
+  if (a.k <= 8) return launch_router_impl<8>(x, w, a, sms, s);
+  return launch_router_impl<16>(x, w, a, sms, s);
+}
+
+}  // namespace lmoe

@@ -79,6 +79,6 @@ def test_strings_and_stages(lib):
     assert lib.latentmoe_strerror(capi.ERR_TIMEOUT) == b"a bounded device wait timed out"
     n = lib.latentmoe_num_stages()
     names = [lib.latentmoe_stage_name(i).decode() for i in range(n)]
-    assert names == ["router_gemm", "route_topk", "sort", "down_proj", "expert_gate_up",
+    assert names == ["router", "replay_gates", "sort", "down_proj", "expert_gate_up",
                      "expert_down", "combine", "shared_gate_up", "up_proj"]
     assert lib.latentmoe_stage_name(n) is None
