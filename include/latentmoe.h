@@ -57,7 +57,7 @@ typedef struct {
 } latentmoe_dims;
 
 /* Device pointers to the weights, all bf16 except b_r (fp32).
- *   w_r  [E, d]        router               b_r [E] (LATENTMOE_ROUTER_BIAS only)
+ *   w_r  [E, d]        router               b_r [E] (with either bias flag)
  *   w_dn [l, d]        latent down          w_up [d, l]   latent up
  *   w_g, w_u [E, F, l] expert gate and up   w_d [E, l, F] expert down
  *   w_gs, w_us [F_s, d], w_ds [d, F_s]      shared expert (F_s > 0 only)
@@ -78,7 +78,14 @@ typedef struct {
 enum {
   LATENTMOE_RENORM = 1u,      /* divide the k gates of a token by their sum */
   LATENTMOE_ROUTER_BIAS = 2u, /* add b_r to the logits (selection and softmax) */
-  LATENTMOE_OUT_FP32 = 4u     /* forward output y is fp32 instead of bf16 */
+  LATENTMOE_OUT_FP32 = 4u,    /* forward output y is fp32 instead of bf16 */
+  LATENTMOE_SELECT_BIAS = 8u  /* b_r moves only the top-k choice (ranks L + b);
+                                 gates stay the unbiased softmax; exported
+                                 logits are unbiased. The selection-only reading
+                                 of the loss-free balancer named in "The Training
+                                 and RL Infrastructure Behind MAI-Thinking-1",
+                                 section "Sharding and parallelism". Not together
+                                 with LATENTMOE_ROUTER_BIAS. */
 };
 
 enum {
@@ -188,6 +195,23 @@ int latentmoe_route_from_logits_static(const float* logits, int64_t T, int64_t E
                                        float* gates, int32_t* counts,
                                        int32_t* offsets, int32_t* perm, int32_t* pos,
                                        latentmoe_stream_t stream);
+
+/* Load-balancing statistics of the last forward on this handle ("The
+ * Training and RL Infrastructure Behind MAI-Thinking-1", section "Sharding
+ * and parallelism": a global-batch load-balancing loss aggregated across
+ * data-parallel workers and micro-batches; "Frontier Pre-training at
+ * Microsoft AI", section "Reducing per-expert overhead": batched across
+ * layers). The loss formula is not given, so the entry returns the
+ * per-batch statistics it is built from, ready to be summed across batches,
+ * ranks and layers:
+ *   counts [E] int32      slots routed to each expert (sum = T*k)
+ *   prob_sum [E] fp32     sum over tokens of the router's softmax
+ *                         probability of each expert (sum = T)
+ * Either pointer may be NULL. Device pointers; enqueued on `stream`;
+ * deterministic. After a replay forward with given gates (no router run)
+ * prob_sum describes the last routed forward's logits. */
+int latentmoe_lbl_stats(latentmoe_t h, float* prob_sum, int32_t* counts,
+                        latentmoe_stream_t stream);
 
 /* Copy the routing state of the last forward on this handle into caller
  * device buffers (each may be NULL): logits [T, E] fp32 (bias included),

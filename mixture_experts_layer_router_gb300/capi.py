@@ -26,6 +26,7 @@ ERR_OUT_OF_MEMORY = -7
 RENORM = 1
 ROUTER_BIAS = 2
 OUT_FP32 = 4
+SELECT_BIAS = 8
 
 STATUS_TIMEOUT = 1
 STATUS_BAD_EXPERT = 2
@@ -57,6 +58,7 @@ SIGNATURES = {
     "latentmoe_route_from_logits": (ctypes.c_int, [_c_void_p, _c_void_p, _i64] + [_c_void_p] * 7),
     "latentmoe_route_from_logits_static": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_int,
                                                           ctypes.c_uint32] + [_c_void_p] * 7),
+    "latentmoe_lbl_stats": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "latentmoe_get_routing": (ctypes.c_int, [_c_void_p] + [_c_void_p] * 7 + [_c_void_p]),
     "latentmoe_get_status": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "latentmoe_set_profiling": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
@@ -126,12 +128,12 @@ class LatentMoE:
 
     def __init__(self, d: int, l: int, E: int, k: int, F: int, Fs: int = 0,
                  max_tokens: int = 1, renorm: bool = False, router_bias: bool = False,
-                 out_fp32: bool = False):
+                 out_fp32: bool = False, select_bias: bool = False):
         lib = load()
         self.dims = latentmoe_dims(d, l, E, F, Fs, max_tokens)
         self.k = k
         self.flags = (RENORM if renorm else 0) | (ROUTER_BIAS if router_bias else 0) | \
-            (OUT_FP32 if out_fp32 else 0)
+            (OUT_FP32 if out_fp32 else 0) | (SELECT_BIAS if select_bias else 0)
         h = _c_void_p()
         check(lib.latentmoe_create(ctypes.byref(self.dims), k, self.flags, ctypes.byref(h)),
               "latentmoe_create")
@@ -219,6 +221,16 @@ class LatentMoE:
                            ("logits", "idx", "gates", "counts", "offsets", "perm", "pos")),
             _stream(stream)), "latentmoe_get_routing")
         return out
+
+    def lbl_stats(self, device, stream=None):
+        """(prob_sum [E] fp32, counts [E] int32) of the last forward."""
+        import torch
+        E = self.dims.num_experts
+        ps = torch.empty((E,), dtype=torch.float32, device=device)
+        cn = torch.empty((E,), dtype=torch.int32, device=device)
+        check(load().latentmoe_lbl_stats(self.handle, ps.data_ptr(), cn.data_ptr(),
+                                         _stream(stream)), "latentmoe_lbl_stats")
+        return ps, cn
 
     def status(self) -> int:
         v = ctypes.c_uint32(0)

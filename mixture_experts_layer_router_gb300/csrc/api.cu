@@ -131,6 +131,7 @@ struct latentmoe {
   int* cnt = nullptr;
   int* cbase = nullptr;
   int* counts = nullptr;
+  float* lbl_partial = nullptr;
   int* offsets = nullptr;
   int* perm = nullptr;
   int* pos = nullptr;
@@ -197,8 +198,9 @@ int run_sort(latentmoe* h, int T, cudaStream_t s) {
 // gates -> counts, offsets, perm, pos (workspace buffers).
 int run_routing(latentmoe* h, const float* logits, int T, cudaStream_t s, int slot_base) {
   const int E = static_cast<int>(h->dims.num_experts);
+  const float* sel_bias = (h->flags & LATENTMOE_SELECT_BIAS) ? h->w.b_r : nullptr;
   LMOE_CK(h, lmoe::launch_route_topk(logits, T, E, h->k, (h->flags & LATENTMOE_RENORM) ? 1 : 0,
-                                     h->idx, h->gates, s));
+                                     sel_bias, h->idx, h->gates, s));
   h->launches += 1;
   record(h, slot_base, 2, s);
   const int r = run_sort(h, T, s);
@@ -237,7 +239,9 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   if (dims == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   const latentmoe_dims d = *dims;
   if (flags & ~static_cast<uint32_t>(LATENTMOE_RENORM | LATENTMOE_ROUTER_BIAS |
-                                     LATENTMOE_OUT_FP32))
+                                     LATENTMOE_OUT_FP32 | LATENTMOE_SELECT_BIAS))
+    return LATENTMOE_ERR_INVALID_ARG;
+  if ((flags & LATENTMOE_ROUTER_BIAS) && (flags & LATENTMOE_SELECT_BIAS))
     return LATENTMOE_ERR_INVALID_ARG;
   if (d.num_experts < 1 || d.max_tokens < 1 || d.hidden < 1 || d.latent < 1 || d.ffn < 1 ||
       d.shared_ffn < 0)
@@ -282,6 +286,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
                o_pos = take(S * 4);
   const size_t o_cnt = take(nb_ints * 4), o_cbase = take(nb_ints * 4);
   const size_t o_counts = take(E * 4), o_offsets = take((E + 1) * 4);
+  const size_t o_lbl = take(((T + lmoe::kLblTokens - 1) / lmoe::kLblTokens) * E * 4);
   const size_t o_zp = take(S * l * 2), o_h = take(S * F * 2), o_o = take(S * l * 2);
   const size_t o_c = take(T * l * 2), o_sh = take(Fs > 0 ? T * Fs * 2 : 16);
   const size_t o_status = take(16);
@@ -300,6 +305,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->cnt = reinterpret_cast<int*>(base + o_cnt);
   h->cbase = reinterpret_cast<int*>(base + o_cbase);
   h->counts = reinterpret_cast<int*>(base + o_counts);
+  h->lbl_partial = reinterpret_cast<float*>(base + o_lbl);
   h->offsets = reinterpret_cast<int*>(base + o_offsets);
   h->zp = reinterpret_cast<__nv_bfloat16*>(base + o_zp);
   h->hb = reinterpret_cast<__nv_bfloat16*>(base + o_h);
@@ -332,7 +338,7 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   if (h == nullptr || w == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   const latentmoe_dims& d = h->dims;
   const bool shared = d.shared_ffn > 0;
-  const bool bias = (h->flags & LATENTMOE_ROUTER_BIAS) != 0;
+  const bool bias = (h->flags & (LATENTMOE_ROUTER_BIAS | LATENTMOE_SELECT_BIAS)) != 0;
   if (!w->w_r || !w->w_dn || !w->w_g || !w->w_u || !w->w_d || !w->w_up)
     return LATENTMOE_ERR_INVALID_ARG;
   if (bias && !w->b_r) return LATENTMOE_ERR_INVALID_ARG;
@@ -476,7 +482,8 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     ra.k = k;
     ra.renorm = (h->flags & LATENTMOE_RENORM) ? 1 : 0;
     ra.kb = dd / lmoe::kRBK;
-    ra.bias = (h->flags & LATENTMOE_ROUTER_BIAS) ? h->w.b_r : nullptr;
+    ra.bias = (h->flags & (LATENTMOE_ROUTER_BIAS | LATENTMOE_SELECT_BIAS)) ? h->w.b_r : nullptr;
+    ra.bias_select = (h->flags & LATENTMOE_SELECT_BIAS) ? 1 : 0;
     ra.logits = h->logits;
     ra.idx = h->idx;
     ra.gates = h->gates;
@@ -654,6 +661,8 @@ int latentmoe_route_from_logits(latentmoe_t h, const float* logits, int64_t T, i
   if (h == nullptr || logits == nullptr || idx == nullptr || gates == nullptr)
     return LATENTMOE_ERR_INVALID_ARG;
   if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  // a selection-only bias comes with the weights
+  if ((h->flags & LATENTMOE_SELECT_BIAS) && !h->loaded) return LATENTMOE_ERR_NOT_LOADED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
   LMOE_CK(h, cudaSetDevice(h->device));
   const int r = run_routing(h, logits, static_cast<int>(T), s, 0);
@@ -688,6 +697,24 @@ int latentmoe_get_routing(latentmoe_t h, float* logits, int32_t* idx, float* gat
   if (offsets) LMOE_CK(h, cudaMemcpyAsync(offsets, h->offsets, (E + 1) * 4, dd, s));
   if (perm) LMOE_CK(h, cudaMemcpyAsync(perm, h->perm, S * 4, dd, s));
   if (pos) LMOE_CK(h, cudaMemcpyAsync(pos, h->pos, S * 4, dd, s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_lbl_stats(latentmoe_t h, float* prob_sum, int32_t* counts,
+                        latentmoe_stream_t st) {
+  if (h == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (h->last_T == 0) return LATENTMOE_ERR_NOT_LOADED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const int E = static_cast<int>(h->dims.num_experts);
+  if (prob_sum) {
+    LMOE_CK(h, lmoe::launch_lbl_prob_sum(h->logits, static_cast<int>(h->last_T), E,
+                                         h->lbl_partial, prob_sum, s));
+    h->launches += 2;
+  }
+  if (counts)
+    LMOE_CK(h, cudaMemcpyAsync(counts, h->counts, static_cast<size_t>(E) * 4,
+                               cudaMemcpyDeviceToDevice, s));
   return LATENTMOE_OK;
 }
 

@@ -40,8 +40,15 @@ cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, Route
                                cudaStream_t s);
 
 // Softmax over E and stable top-k per token: idx [T,k] int32, gates [T,k].
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
-                              float* gates, cudaStream_t s);
+// With sel_bias, the choice ranks logits + bias; gates stay unbiased.
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm,
+                              const float* sel_bias, int* idx, float* gates, cudaStream_t s);
+
+// prob_sum[e] = sum_t softmax(logits_t)_e, deterministic. Scratch: partial
+// [ceil(T / kLblTokens), E] floats. Two launches.
+constexpr int kLblTokens = 256;
+cudaError_t launch_lbl_prob_sum(const float* logits, int T, int E, float* partial, float* out,
+                                cudaStream_t s);
 
 // Router replay: gates[t,j] = softmax(logits[t])[idx[t,j]] (0 for ids outside
 // [0, E)), divided by their sum with renorm.

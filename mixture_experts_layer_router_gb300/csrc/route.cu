@@ -25,6 +25,7 @@ namespace lmoe {
 template <int VPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int renorm,
+                                                         const float* __restrict__ sel_bias,
                                                          int* __restrict__ idx,
                                                          float* __restrict__ gates) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -50,6 +51,13 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
 
+  // ranking keys: the logits, or logits + bias for a selection-only bias
+  float key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (sel_bias != nullptr && e < E) ? v[i] + sel_bias[e] : v[i];
+  }
   uint32_t taken = 0;
   float gsel[16];
   int isel[16];
@@ -59,25 +67,29 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     if (j < k) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
+      float bl = -INFINITY;  // the logit of the best key
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
+        if (e < E && !((taken >> i) & 1u) && (key[i] > bv || (key[i] == bv && e < bi))) {
+          bv = key[i];
           bi = e;
+          bl = v[i];
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
         if (ov > bv || (ov == bv && oi < bi)) {
           bv = ov;
           bi = oi;
+          bl = ol;
         }
       }
       if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float g = expf(bv - m) / s;
+      const float g = expf(bl - m) / s;
       gsel[j] = g;
       isel[j] = bi;
       gsum += g;
@@ -165,20 +177,102 @@ cudaError_t launch_replay_gates(const float* logits, int T, int E, const int* id
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int* idx,
-                              float* gates, cudaStream_t s) {
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm,
+                              const float* sel_bias, int* idx, float* gates, cudaStream_t s) {
   const int blocks = (T + 7) / 8;
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+    route_topk_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, sel_bias, idx, gates);
   else if (vpl <= 2)
-    route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+    route_topk_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, sel_bias, idx, gates);
   else if (vpl <= 4)
-    route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+    route_topk_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, sel_bias, idx, gates);
   else if (vpl <= 8)
-    route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+    route_topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, sel_bias, idx, gates);
   else
-    route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, idx, gates);
+    route_topk_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, k, renorm, sel_bias, idx, gates);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Load-balancing statistics: prob_sum[e] = sum over tokens of softmax(L_t)_e,
+// with the softmax of route_topk_kernel (same max and sum reductions). Block b
+// takes kLblTokens tokens, 32 per warp in token order; each lane accumulates
+// its experts over its warp's tokens, the warps' partials are added in warp
+// order, and a second kernel adds the blocks' partials in block order, so the
+// result does not depend on scheduling.
+template <int VPL>
+__global__ void __launch_bounds__(256) lbl_partial_kernel(const float* __restrict__ logits, int T,
+                                                          int E, float* __restrict__ partial) {
+  __shared__ float wsum[8][512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) acc[i] = 0.0f;
+  const int t0 = blockIdx.x * kLblTokens + warp * (kLblTokens / 8);
+  for (int tt = 0; tt < kLblTokens / 8; ++tt) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    const float* row = logits + static_cast<long long>(t) * E;
+    float v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      float x = (e < E) ? row[e] : -INFINITY;
+      v[i] = (x != x) ? -INFINITY : x;
+    }
+    float m = v[0];
+#pragma unroll
+    for (int i = 1; i < VPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E) acc[i] += expf(v[i] - m) / s;
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) wsum[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float tot = 0.0f;
+    for (int w = 0; w < 8; ++w) tot += wsum[w][e];
+    partial[static_cast<long long>(blockIdx.x) * E + e] = tot;
+  }
+}
+
+__global__ void lbl_reduce_kernel(const float* __restrict__ partial, int nb, int E,
+                                  float* __restrict__ out) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  float tot = 0.0f;
+  for (int b = 0; b < nb; ++b) tot += partial[static_cast<long long>(b) * E + e];
+  out[e] = tot;
+}
+
+cudaError_t launch_lbl_prob_sum(const float* logits, int T, int E, float* partial, float* out,
+                                cudaStream_t s) {
+  const int nb = (T + kLblTokens - 1) / kLblTokens;
+  const int vpl = (E + 31) / 32;
+  if (vpl <= 1)
+    lbl_partial_kernel<1><<<nb, 256, 0, s>>>(logits, T, E, partial);
+  else if (vpl <= 2)
+    lbl_partial_kernel<2><<<nb, 256, 0, s>>>(logits, T, E, partial);
+  else if (vpl <= 4)
+    lbl_partial_kernel<4><<<nb, 256, 0, s>>>(logits, T, E, partial);
+  else if (vpl <= 8)
+    lbl_partial_kernel<8><<<nb, 256, 0, s>>>(logits, T, E, partial);
+  else
+    lbl_partial_kernel<16><<<nb, 256, 0, s>>>(logits, T, E, partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  lbl_reduce_kernel<<<(E + 127) / 128, 128, 0, s>>>(partial, nb, E, out);
   return cudaGetLastError();
 }
 

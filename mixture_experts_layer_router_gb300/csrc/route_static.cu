@@ -80,7 +80,8 @@ extern "C" int latentmoe_route_from_logits_static(const float* logits, int64_t T
   // has to start at zero
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return LATENTMOE_ERR_CUDA;
   if (lmoe::launch_route_topk(logits, static_cast<int>(T), static_cast<int>(E), top_k,
-                              (flags & LATENTMOE_RENORM) ? 1 : 0, idx, gates, s) != cudaSuccess)
+                              (flags & LATENTMOE_RENORM) ? 1 : 0, nullptr, idx, gates,
+                              s) != cudaSuccess)
     return LATENTMOE_ERR_CUDA;
   if (lmoe::launch_sort(idx, static_cast<int>(S), top_k, static_cast<int>(E), cnt, cbase, counts,
                         offsets, perm, pos, status, s) != cudaSuccess)

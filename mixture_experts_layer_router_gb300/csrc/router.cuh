@@ -55,6 +55,7 @@ struct RouterArgs {
   int kb;                  // d / kRBK
   int stages;              // shared-memory stages (set by the launcher)
   const float* bias;       // [E] or null
+  int bias_select;         // 0: bias is part of the logits; 1: it only moves the top-k choice
   float* logits;           // [T, E] fp32 out
   int* idx;                // [T, k]
   float* gates;            // [T, k]
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float x = __uint_as_float(v[i]);
-            if (e0 + i < a.E && a.bias != nullptr) x += a.bias[e0 + i];
+            if (e0 + i < a.E && a.bias != nullptr && !a.bias_select) x += a.bias[e0 + i];
             v[i] = __float_as_uint(x);
           }
           if (row_ok) {
@@ -283,7 +284,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             float x = __uint_as_float(v[i]);
             x = (x != x) ? -INFINITY : x;
             m = fmaxf(m, x);
-            topk_insert<KMAX>(sv, si, x, e);
+            // the ranking key: the logit, or logit + bias for a selection-only bias
+            const float xs = a.bias_select ? x + a.bias[e] : x;
+            topk_insert<KMAX>(sv, si, xs, e);
           }
         }
       }
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           const int e = c * 32 + sub * 8 + j;
           if (e < a.E) {
             float x = __uint_as_float(v[j]);
-            if (a.bias != nullptr) x += a.bias[e];
+            if (a.bias != nullptr && !a.bias_select) x += a.bias[e];
             x = (x != x) ? -INFINITY : x;
             p[j] += expf(x - m);
           }
@@ -348,7 +351,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
         for (int j = 0; j < KMAX; ++j) {
           g[j] = 0.0f;
           if (j < k) {
-            g[j] = expf(sv[j] - m) / ssum;
+            // with a selection-only bias the list holds biased keys: take the
+            // logit itself from the row this CTA exported
+            float lx = sv[j];
+            if (a.bias_select) {
+              lx = lrow[si[j]];
+              lx = (lx != lx) ? -INFINITY : lx;
+            }
+            g[j] = expf(lx - m) / ssum;
             gsum += g[j];
           }
         }

@@ -194,11 +194,22 @@ def shared_expert(x: np.ndarray, w_gs, w_us, w_ds) -> np.ndarray:
 
 
 def forward(x: np.ndarray, weights: OracleWeights, k: int, renorm: bool = False,
-            logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+            logits: Optional[np.ndarray] = None,
+            select_bias: Optional[np.ndarray] = None,
+            select_logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """The whole layer on x [T, d]; returns every intermediate.
 
     ``logits`` (e.g. the GPU's fp32 router logits) replaces step 1 when given;
     selection and gates then follow from those values exactly.
+
+    ``select_bias`` [E] is the selection-only reading of the loss-free
+    balancer that "The Training and RL Infrastructure Behind MAI-Thinking-1"
+    names without a mechanism (section "Sharding and parallelism"): the bias
+    moves the top-k choice (step 3 ranks L + b) while the gates stay the
+    softmax probabilities of the unbiased logits (steps 2 and 4).
+    ``select_logits`` [T, E] gives that ranking key directly (L + b as another
+    implementation rounded it), so that a comparison can take the choice in
+    the other side's precision.
     """
     x = np.asarray(x, dtype=np.float64)
     E = weights.num_experts
@@ -207,7 +218,12 @@ def forward(x: np.ndarray, weights: OracleWeights, k: int, renorm: bool = False,
     else:
         L = np.asarray(logits, dtype=np.float64)
     p = softmax_rows(L)
-    idx = top_k_stable(L, k)
+    if select_logits is not None:
+        idx = top_k_stable(np.asarray(select_logits, dtype=np.float64), k)
+    elif select_bias is None:
+        idx = top_k_stable(L, k)
+    else:
+        idx = top_k_stable(L + np.asarray(select_bias, dtype=np.float64)[None, :], k)
     g = select_gates(p, idx, renorm)
     z = latent_down(x, weights.w_dn)
     counts, offsets, perm, pos = counting_sort(idx, E)
@@ -254,13 +270,41 @@ def forward_routed(x: np.ndarray, weights: OracleWeights, idx: np.ndarray,
             "pos": pos, "c": c, "y": y}
 
 
-def route(logits: np.ndarray, E: int, k: int, renorm: bool = False) -> Dict[str, np.ndarray]:
+def route(logits: np.ndarray, E: int, k: int, renorm: bool = False,
+          select_bias: Optional[np.ndarray] = None,
+          select_logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """Steps 2-4 and 6 from given logits: the routing half of the layer."""
     L = np.asarray(logits, dtype=np.float64)
     p = softmax_rows(L)
-    idx = top_k_stable(L, k)
+    if select_logits is not None:
+        idx = top_k_stable(np.asarray(select_logits, dtype=np.float64), k)
+    elif select_bias is None:
+        idx = top_k_stable(L, k)
+    else:
+        idx = top_k_stable(L + np.asarray(select_bias, dtype=np.float64)[None, :], k)
     g = select_gates(p, idx, renorm)
     counts, offsets, perm, pos = counting_sort(idx, E)
     return {"idx": idx, "gates": g, "counts": counts, "offsets": offsets,
             "perm": perm, "pos": pos}
 
+
+
+def lbl_stats(logits: np.ndarray, idx: np.ndarray, E: int):
+    """Load-balancing statistics of one batch: slots per expert and the sum
+    over tokens of each expert's router probability.
+
+    "The Training and RL Infrastructure Behind MAI-Thinking-1" (section
+    "Sharding and parallelism") uses a global-batch load-balancing loss,
+    aggregated across data-parallel workers and micro-batches; "Frontier
+    Pre-training at Microsoft AI" (section "Reducing per-expert overhead")
+    batches it across layers. The loss formula and its coefficient are not on
+    the pages, so these are the per-batch statistics such a loss is built
+    from: counts n_e (sum them over batches, divide by the total slots for
+    f_e) and prob_sum_e = sum_t softmax(L_t)_e (sum over batches, divide by
+    the total tokens for the mean probability P_e).
+    """
+    p = softmax_rows(np.asarray(logits, dtype=np.float64))
+    counts = np.zeros(E, dtype=np.int64)
+    for e in np.asarray(idx).ravel():
+        counts[e] += 1
+    return counts, p.sum(axis=0)

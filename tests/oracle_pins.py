@@ -342,8 +342,44 @@ def check_replay(ref):
             assert np.array_equal(got["pos"], np.array(bf["pos"]))
 
 
+def check_select_bias(ref):
+    """Selection-only bias: zero bias changes nothing; a bias moves only the
+    choice (gates stay unbiased softmax probabilities); a dominant bias forces
+    its expert into every token's top-k."""
+    w = tiny_layer(71, T=9, E=6, k=2)
+    W = oracle_weights(ref, w)
+    base = ref.forward(w["x"], W, 2)
+    zero = ref.forward(w["x"], W, 2, select_bias=np.zeros(6))
+    np.testing.assert_allclose(zero["y"], base["y"], rtol=0, atol=0)
+    b = np.zeros(6)
+    b[4] = 1e6
+    forced = ref.forward(w["x"], W, 2, select_bias=b)
+    assert np.all(forced["idx"][:, 0] == 4)
+    np.testing.assert_allclose(forced["gates"][:, 0], base["p"][:, 4], rtol=1e-14)
+    # the second choice is the unbiased top-1 unless that was expert 4
+    top1 = np.argsort(-base["logits"], axis=1, kind="stable")
+    want2 = np.where(top1[:, 0] == 4, top1[:, 1], top1[:, 0])
+    assert np.array_equal(forced["idx"][:, 1], want2)
+
+
+def check_lbl_stats(ref):
+    """Counts sum to T*k and match a direct tally; probability sums add up to
+    T (each token's softmax sums to 1) and equal a per-token scipy softmax."""
+    rng = np.random.default_rng(12)
+    T, E, k = 40, 7, 3
+    L = rng.standard_normal((T, E)) * 2
+    idx = ref.top_k_stable(L, k)
+    counts, psum = ref.lbl_stats(L, idx, E)
+    assert counts.sum() == T * k
+    tally = [sum(1 for t in range(T) for j in range(k) if idx[t, j] == e) for e in range(E)]
+    assert counts.tolist() == tally
+    np.testing.assert_allclose(psum.sum(), T, rtol=1e-13)
+    np.testing.assert_allclose(psum, _softmax(L).sum(axis=0), rtol=1e-13)
+
+
 ALL_CHECKS = [
     check_brute_force, check_closed_forms, check_tie_break, check_dense_sandwich,
     check_full_mixture, check_gates, check_counting_sort, check_zero_input,
     check_token_permutation, check_expert_permutation, check_shared_only, check_replay,
+    check_select_bias, check_lbl_stats,
 ]

@@ -49,6 +49,7 @@ def _dims(**kw):
     (dict(num_experts=0), 1, 0, capi.ERR_INVALID_ARG),
     (dict(shared_ffn=-128), 2, 0, capi.ERR_INVALID_ARG),
     (dict(), 2, 64, capi.ERR_INVALID_ARG),                # unknown flag bit
+    (dict(), 2, 2 | 8, capi.ERR_INVALID_ARG),             # both bias modes
     (dict(hidden=200), 2, 0, capi.ERR_UNSUPPORTED),       # not a multiple of 128
     (dict(latent=64), 2, 0, capi.ERR_UNSUPPORTED),
     (dict(ffn=100), 2, 0, capi.ERR_UNSUPPORTED),
