@@ -1,0 +1,124 @@
+"""FP8 E4M3 forward of the expert FFNs in the oracle (test infrastructure).
+
+Only ``tests/`` and ``bench.py``'s CPU legs may import this module; it shares
+no code with the CUDA library.
+
+"The Training and RL Infrastructure Behind MAI-Thinking-1", section
+"2. Numerics": forward GEMMs run in FP8 E4M3, and every FP8 operation uses
+delayed scaling with a 1,024-step history of the absolute maximum. This
+module restates that for the two expert GEMMs of the layer:
+
+- E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities, the
+  largest finite value 448, subnormals down to 2^-9. Rounding is to nearest,
+  ties to even; magnitudes above 448 saturate to 448.
+- A tensor t with scale s is stored as q = E4M3(t / s) and stands for q * s.
+- Weights (static): s = amax(W_e) / 448 per expert matrix.
+- Activations: z (input of gate/up) and h (input of down) use per-tensor
+  scales from delayed scaling; the scales are inputs here (the GPU reports
+  the ones it used).
+- g = (q_z q_g^T) s_z s_g, u = (q_z q_u^T) s_z s_u, h = SiLU(g) u,
+  o = (q_h q_d^T) s_h s_d.
+
+Readings where the pages are silent: scales are per tensor, and per expert
+for the expert weights; the history starts empty and a scale of 1 is used
+until it holds a non-zero maximum.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+
+from oracle import latentmoe_ref as ref
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest E4M3 value (ties to even), saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    # spacing of representable values: 2^(e-3) in binade e >= -6, 2^-9 below
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -9)))
+    e = np.maximum(e, -6.0)
+    q = np.exp2(e - 3.0)
+    r = np.round(a / q) * q  # np.round rounds half to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(x < 0, -r, r)
+
+
+def e4m3_values() -> np.ndarray:
+    """All non-negative finite E4M3 values, from the bit layout."""
+    vals = []
+    for exp in range(16):
+        for man in range(8):
+            if exp == 15 and man == 7:
+                continue  # the NaN code
+            if exp == 0:
+                vals.append(man * 2.0 ** -9)
+            else:
+                vals.append((1.0 + man / 8.0) * 2.0 ** (exp - 7))
+    return np.array(sorted(set(vals)))
+
+
+def weight_scale(w: np.ndarray) -> float:
+    """amax / 448 in fp32, the way the kernel forms it (1 for an all-zero matrix)."""
+    amax = np.float32(np.max(np.abs(w))) if w.size else np.float32(0)
+    if amax == 0:
+        return 1.0
+    return float(np.float32(amax) / np.float32(E4M3_MAX))
+
+
+def quantize_weight(w: np.ndarray):
+    """(codes as float64 values, scale): the codes are E4M3(fp32(w) * fp32(1/s)),
+    the fp32 operations the kernel uses, so the codes match it exactly."""
+    s = weight_scale(w)
+    inv = np.float32(1.0) / np.float32(s)
+    prod = (np.asarray(w, dtype=np.float32) * inv).astype(np.float64)
+    return round_e4m3(prod), s
+
+
+def quantize_act(t: np.ndarray, s: float) -> np.ndarray:
+    """Activation codes E4M3(t * (1/s)); t is the float64 oracle value."""
+    inv = float(np.float32(1.0) / np.float32(s))
+    return round_e4m3(np.asarray(t, dtype=np.float64) * inv)
+
+
+def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s_h: float,
+                renorm: bool = False, logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The layer with FP8 E4M3 expert GEMMs; everything else as ref.forward."""
+    x = np.asarray(x, dtype=np.float64)
+    E = weights.num_experts
+    L = ref.router_logits(x, weights.w_r, weights.b_r) if logits is None else \
+        np.asarray(logits, dtype=np.float64)
+    p = ref.softmax_rows(L)
+    idx = ref.top_k_stable(L, k)
+    g = ref.select_gates(p, idx, renorm)
+    z = ref.latent_down(x, weights.w_dn)
+    counts, offsets, perm, pos = ref.counting_sort(idx, E)
+    qz = quantize_act(z, s_z)
+    H = np.zeros((perm.shape[0], z.shape[1]), dtype=np.float64)
+    h_amax = 0.0
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        w_g, w_u, w_d = weights.expert(e)
+        qg, sg = quantize_weight(w_g)
+        qu, su = quantize_weight(w_u)
+        qd, sd = quantize_weight(w_d)
+        zq = qz[perm[lo:hi]]
+        gate = (zq @ qg.T) * (s_z * sg)
+        up = (zq @ qu.T) * (s_z * su)
+        h = ref.silu(gate) * up
+        h_amax = max(h_amax, float(np.abs(h).max()))
+        qh = quantize_act(h, s_h)
+        H[lo:hi] = (qh @ qd.T) * (s_h * sd)
+    c = ref.combine(H, g, pos)
+    y = ref.latent_up(c, weights.w_up)
+    if weights.w_gs is not None:
+        y = y + ref.shared_expert(x, weights.w_gs, weights.w_us, weights.w_ds)
+    # the maxima delayed scaling records for the next step's scales
+    z_amax = float(np.abs(z[perm]).max()) if perm.size else 0.0
+    return {"idx": idx, "gates": g, "counts": counts, "pos": pos, "perm": perm, "y": y,
+            "z_amax": z_amax, "h_amax": h_amax}
