@@ -22,6 +22,11 @@ module restates that for the two expert GEMMs of the layer:
 Readings where the pages are silent: scales are per tensor, and per expert
 for the expert weights; the history starts empty and a scale of 1 is used
 until it holds a non-zero maximum.
+
+Delayed scaling (DelayedScaling below): forward n quantizes with the scale
+made from the maxima of forwards n-1024 .. n-1 (s = max / 448, formed in
+fp32); the maximum forward n records enters the history afterwards. A window
+whose maxima are all zero leaves the scale as it was.
 """
 from __future__ import annotations
 
@@ -61,6 +66,30 @@ def e4m3_values() -> np.ndarray:
     return np.array(sorted(set(vals)))
 
 
+HISTORY = 1024
+
+
+class DelayedScaling:
+    """Scales of a few activation tensors from a ring of recorded maxima."""
+
+    def __init__(self, n: int, length: int = HISTORY):
+        self.length = length
+        self.hist = np.zeros((n, length), dtype=np.float32)
+        self.scales = np.ones(n, dtype=np.float32)
+        self.steps = 0
+
+    def record(self, amax) -> np.ndarray:
+        """Enter one forward's maxima (fp32) and return the next scales."""
+        amax = np.asarray(amax, dtype=np.float32)
+        self.hist[:, self.steps % self.length] = amax
+        self.steps += 1
+        m = self.hist.max(axis=1)
+        for i in range(m.shape[0]):
+            if m[i] > 0:
+                self.scales[i] = np.float32(m[i]) / np.float32(E4M3_MAX)
+        return self.scales.copy()
+
+
 def weight_scale(w: np.ndarray) -> float:
     """amax / 448 in fp32, the way the kernel forms it (1 for an all-zero matrix)."""
     amax = np.float32(np.max(np.abs(w))) if w.size else np.float32(0)
@@ -85,8 +114,15 @@ def quantize_act(t: np.ndarray, s: float) -> np.ndarray:
 
 
 def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s_h: float,
-                renorm: bool = False, logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
-    """The layer with FP8 E4M3 expert GEMMs; everything else as ref.forward."""
+                renorm: bool = False, logits: Optional[np.ndarray] = None,
+                z_codes: Optional[np.ndarray] = None,
+                h_codes: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The layer with FP8 E4M3 expert GEMMs; everything else as ref.forward.
+
+    z_codes [T*k, l] / h_codes [T*k, F] (E4M3 code values, slot order), when
+    given, replace the codes this function would form for z and h: the
+    expert GEMMs are then evaluated on exactly those codes. The returned
+    "z_q" and "h_q" are the codes used, and "h" the unquantized h."""
     x = np.asarray(x, dtype=np.float64)
     E = weights.num_experts
     L = ref.router_logits(x, weights.w_r, weights.b_r) if logits is None else \
@@ -96,8 +132,12 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
     g = ref.select_gates(p, idx, renorm)
     z = ref.latent_down(x, weights.w_dn)
     counts, offsets, perm, pos = ref.counting_sort(idx, E)
-    qz = quantize_act(z, s_z)
+    zq_slots = quantize_act(z, s_z)[perm] if z_codes is None else \
+        np.asarray(z_codes, dtype=np.float64)
     H = np.zeros((perm.shape[0], z.shape[1]), dtype=np.float64)
+    F = weights.expert(0)[0].shape[0]
+    h_all = np.zeros((perm.shape[0], F), dtype=np.float64)
+    hq_all = np.zeros((perm.shape[0], F), dtype=np.float64)
     h_amax = 0.0
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
@@ -107,18 +147,22 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         qg, sg = quantize_weight(w_g)
         qu, su = quantize_weight(w_u)
         qd, sd = quantize_weight(w_d)
-        zq = qz[perm[lo:hi]]
+        zq = zq_slots[lo:hi]
         gate = (zq @ qg.T) * (s_z * sg)
         up = (zq @ qu.T) * (s_z * su)
         h = ref.silu(gate) * up
         h_amax = max(h_amax, float(np.abs(h).max()))
-        qh = quantize_act(h, s_h)
+        qh = quantize_act(h, s_h) if h_codes is None else \
+            np.asarray(h_codes[lo:hi], dtype=np.float64)
+        h_all[lo:hi] = h
+        hq_all[lo:hi] = qh
         H[lo:hi] = (qh @ qd.T) * (s_h * sd)
     c = ref.combine(H, g, pos)
     y = ref.latent_up(c, weights.w_up)
     if weights.w_gs is not None:
         y = y + ref.shared_expert(x, weights.w_gs, weights.w_us, weights.w_ds)
     # the maxima delayed scaling records for the next step's scales
-    z_amax = float(np.abs(z[perm]).max()) if perm.size else 0.0
-    return {"idx": idx, "gates": g, "counts": counts, "pos": pos, "perm": perm, "y": y,
-            "z_amax": z_amax, "h_amax": h_amax}
+    z_amax = float(np.abs(z).max()) if z.size else 0.0
+    return {"idx": idx, "gates": g, "counts": counts, "offsets": offsets, "pos": pos,
+            "perm": perm, "y": y, "z_amax": z_amax, "h_amax": h_amax, "z_q": zq_slots,
+            "h": h_all, "h_q": hq_all}

@@ -200,3 +200,30 @@ def test_planted_fp8_mistake_is_caught(name, monkeypatch):
         except Exception as exc:
             caught.append(check.__name__)
     assert caught, f"mutation {name} passed every FP8 pin"
+
+
+def test_delayed_scaling_window():
+    """The scale follows the largest maximum of the last 1024 forwards: a
+    spike at forward 0 sets it for exactly 1024 steps, then it falls back."""
+    ds = fp8.DelayedScaling(2)
+    assert ds.scales.tolist() == [1.0, 1.0]
+    s = ds.record([896.0, 0.0])
+    assert s[0] == 2.0 and s[1] == 1.0  # zero maxima keep the initial scale
+    for n in range(1, 1024):
+        s = ds.record([44.8, 4.48])
+        assert s[0] == 2.0 and s[1] == np.float32(np.float32(4.48) / np.float32(448))
+    s = ds.record([44.8, 4.48])  # forward 1024 overwrites the spike
+    assert s[0] == np.float32(np.float32(44.8) / np.float32(448))
+    assert ds.steps == 1025
+
+
+def test_given_codes_reproduce_own_codes():
+    """Passing back the codes the oracle formed itself changes nothing."""
+    w = oracle_pins.tiny_layer(83, T=33, d=16, l=32, E=5, k=2, F=48)
+    W = oracle_pins.oracle_weights(ref, w)
+    a = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003)
+    b = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, z_codes=a["z_q"], h_codes=a["h_q"])
+    assert np.array_equal(a["y"], b["y"])
+    # slot i holds token perm[i]'s latent codes
+    z = ref.latent_down(w["x"], W.w_dn)
+    assert np.array_equal(a["z_q"], fp8.quantize_act(z, 0.01)[a["perm"]])
