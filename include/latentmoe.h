@@ -79,13 +79,15 @@ enum {
   LATENTMOE_RENORM = 1u,      /* divide the k gates of a token by their sum */
   LATENTMOE_ROUTER_BIAS = 2u, /* add b_r to the logits (selection and softmax) */
   LATENTMOE_OUT_FP32 = 4u,    /* forward output y is fp32 instead of bf16 */
-  LATENTMOE_SELECT_BIAS = 8u  /* b_r moves only the top-k choice (ranks L + b);
+  LATENTMOE_SELECT_BIAS = 8u, /* b_r moves only the top-k choice (ranks L + b);
                                  gates stay the unbiased softmax; exported
                                  logits are unbiased. The selection-only reading
                                  of the loss-free balancer named in "The Training
                                  and RL Infrastructure Behind MAI-Thinking-1",
                                  section "Sharding and parallelism". Not together
                                  with LATENTMOE_ROUTER_BIAS. */
+  LATENTMOE_FP8_EXPERTS = 16u /* the expert GEMMs in FP8 E4M3 with delayed
+                                 scaling; see "FP8 E4M3 expert GEMMs" below */
 };
 
 enum {
@@ -105,6 +107,25 @@ enum {
   LATENTMOE_STATUS_BAD_EXPERT = 2u  /* an expert id outside [0, E) reached the sort */
 };
 
+/* FP8 E4M3 expert GEMMs (LATENTMOE_FP8_EXPERTS). "The Training and RL
+ * Infrastructure Behind MAI-Thinking-1", section "2. Numerics": forward
+ * GEMMs in FP8 E4M3, per-tensor scales from a 1,024-step history of absolute
+ * maxima (delayed scaling). E4M3 here: 4 exponent bits (bias 7), 3 mantissa
+ * bits, largest finite 448, rounding to nearest even, saturating. A tensor t
+ * with scale s is stored as codes E4M3(t * (1/s)) and stands for code * s.
+ * - Expert weights: latentmoe_load_weights quantizes each of W_g^e, W_u^e,
+ *   W_d^e with its own scale s = max|W| / 448 (fp32), keeping the codes only
+ *   (half the bytes of bf16).
+ * - Activations: z (the experts' input, written by the down-projection) and
+ *   h (SiLU(gate) * up) are quantized with per-tensor scales s_z, s_h. The
+ *   forward uses the current scales and records max|z| and max|h|; a last
+ *   kernel enters the maxima into a 1024-entry ring per tensor and sets
+ *   s = max(ring) / 448 for the next forward (unchanged while the ring holds
+ *   only zeros). A new handle starts with s = 1 and an empty ring.
+ * - Everything else (router, down- and up-projection, shared expert,
+ *   combine) is as without the flag. */
+#define LATENTMOE_FP8_TENSORS 2 /* scaled activations, in order: z, h */
+
 /* Create a handle on the current device: validates dims, top_k (1..16,
  * <= E) and flags, and allocates the workspace for max_tokens tokens
  * (intermediates z, h, o, c, routing metadata; about
@@ -116,7 +137,8 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags,
 /* Load the weights (device pointers, layouts in latentmoe_weights). The
  * library copies them into memory it owns (one allocation of the weights'
  * size, freed by latentmoe_destroy or the next load) and rewrites the expert
- * weights into contiguous 128-row x 64-column tiles for its grouped GEMMs.
+ * weights into contiguous tiles of 128 rows x 128 bytes for its grouped
+ * GEMMs (64 bf16 columns, or 128 E4M3 codes with LATENTMOE_FP8_EXPERTS).
  * Synchronises the device before and after the copy, so pending writes to
  * the caller's buffers are seen and the caller may free or reuse them as
  * soon as this returns. Errors: INVALID_ARG (NULL pointer that the dims or
@@ -221,6 +243,39 @@ int latentmoe_get_routing(latentmoe_t h, float* logits, int32_t* idx,
                           float* gates, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* pos, latentmoe_stream_t stream);
 
+/* Delayed-scaling state of an E4M3 handle (synchronises the device):
+ * scales[LATENTMOE_FP8_TENSORS] the next forward will use, last_amax[...]
+ * the maxima the last forward recorded, *steps the forwards entered. Host
+ * pointers. UNSUPPORTED without LATENTMOE_FP8_EXPERTS. */
+int latentmoe_get_fp8_state(latentmoe_t h, float* scales, float* last_amax,
+                            int64_t* steps);
+
+/* E4M3 codes of the last forward's z [T*k, l] and h [T*k, F] (slot order,
+ * as latentmoe_get_routing's perm), copied into caller device buffers on
+ * `stream`; either may be NULL. UNSUPPORTED without LATENTMOE_FP8_EXPERTS,
+ * INVALID_ARG before the first forward. */
+int latentmoe_get_fp8_codes(latentmoe_t h, uint8_t* z_codes, uint8_t* h_codes,
+                            latentmoe_stream_t stream);
+
+/* Set the activation scales (host [LATENTMOE_FP8_TENSORS], finite, > 0)
+ * and clear the history, e.g. from a calibration run. Synchronises the
+ * device. UNSUPPORTED without LATENTMOE_FP8_EXPERTS. */
+int latentmoe_set_fp8_scales(latentmoe_t h, const float* scales);
+
+/* Scales of the loaded expert weights: host fp32 [3, E] (W_g, W_u, W_d of
+ * each expert). Synchronises the device. */
+int latentmoe_get_fp8_weight_scales(latentmoe_t h, float* scales);
+
+/* Quantize bf16 src [groups, rows, cols] (device, cols % 16 == 0) to E4M3
+ * with one scale per group, as the expert weights are: scales[g] =
+ * max|src_g| / 448 in fp32 (1 for an all-zero group), codes = E4M3(src *
+ * (1/scales[g])) with the reciprocal and the product rounded to fp32 first.
+ * codes: device uint8 [groups, rows, cols]; scales: device fp32 [groups].
+ * No handle needed. Asynchronous on `stream`. */
+int latentmoe_quantize_e4m3(const void* src, int64_t groups, int64_t rows,
+                            int64_t cols, uint8_t* codes, float* scales,
+                            latentmoe_stream_t stream);
+
 /* Synchronise the device, then read and clear the device status word
  * (LATENTMOE_STATUS_* bits). Returns TIMEOUT or DEVICE_STATUS when bits
  * were set, CUDA on a CUDA error, else OK. */
@@ -264,6 +319,22 @@ int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C,
                                  const int32_t* offsets, int64_t groups,
                                  int64_t M, int64_t N, int64_t K, int mode,
                                  latentmoe_stream_t stream);
+/* The E4M3 grouped GEMM on its own, with codes as inputs. A: codes [M, K];
+ * B: codes [G*N, K] (mode 1) or [2, G*N, K] (mode 2: gate rows, then up
+ * rows); scales: device fp32 [2 + G] (mode 1) or [2 + 2G] (mode 2):
+ * {s_A, s_out, s_B per group (gate groups, then up groups)}.
+ *   mode 1: C bf16 [M, N] = s_A s_Bg (A B_g^T) for the rows of group g
+ *   mode 2: C codes [M, N] = E4M3((SiLU(s_A s_Bg A B_g^T) * (s_A s_Ug A U_g^T))
+ *           / s_out); amax (device, one uint32, caller-zeroed) receives the
+ *           float bits of max |h| over all rows
+ * Groups as in latentmoe_debug_grouped_gemm. K and N multiples of 128.
+ * Synchronises `stream`. */
+int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B,
+                                      const float* scales, void* C, uint32_t* amax,
+                                      const int32_t* offsets, int64_t groups,
+                                      int64_t M, int64_t N, int64_t K, int mode,
+                                      latentmoe_stream_t stream);
+
 /* Device status word of the debug entry points (synchronises, then clears). */
 int latentmoe_debug_status(uint32_t* device_status);
 

@@ -27,6 +27,8 @@ RENORM = 1
 ROUTER_BIAS = 2
 OUT_FP32 = 4
 SELECT_BIAS = 8
+FP8_EXPERTS = 16
+FP8_TENSORS = 2  # scaled activations: z, h
 
 STATUS_TIMEOUT = 1
 STATUS_BAD_EXPERT = 2
@@ -74,6 +76,17 @@ SIGNATURES = {
     "latentmoe_debug_grouped_gemm": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                                     _i64, _i64, _i64, _i64, ctypes.c_int,
                                                     _c_void_p]),
+    "latentmoe_get_fp8_state": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_float),
+                                               ctypes.POINTER(ctypes.c_float),
+                                               ctypes.POINTER(_i64)]),
+    "latentmoe_get_fp8_codes": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "latentmoe_set_fp8_scales": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_float)]),
+    "latentmoe_get_fp8_weight_scales": (ctypes.c_int, [_c_void_p,
+                                                       ctypes.POINTER(ctypes.c_float)]),
+    "latentmoe_quantize_e4m3": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p,
+                                               _c_void_p, _c_void_p]),
+    "latentmoe_debug_grouped_gemm_e4m3": (ctypes.c_int, [_c_void_p] * 6 + [_i64] * 4 +
+                                          [ctypes.c_int, _c_void_p]),
     "latentmoe_debug_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "latentmoe_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64,
                                                     ctypes.POINTER(ctypes.c_uint32)]),
@@ -128,12 +141,13 @@ class LatentMoE:
 
     def __init__(self, d: int, l: int, E: int, k: int, F: int, Fs: int = 0,
                  max_tokens: int = 1, renorm: bool = False, router_bias: bool = False,
-                 out_fp32: bool = False, select_bias: bool = False):
+                 out_fp32: bool = False, select_bias: bool = False, fp8: bool = False):
         lib = load()
         self.dims = latentmoe_dims(d, l, E, F, Fs, max_tokens)
         self.k = k
         self.flags = (RENORM if renorm else 0) | (ROUTER_BIAS if router_bias else 0) | \
-            (OUT_FP32 if out_fp32 else 0) | (SELECT_BIAS if select_bias else 0)
+            (OUT_FP32 if out_fp32 else 0) | (SELECT_BIAS if select_bias else 0) | \
+            (FP8_EXPERTS if fp8 else 0)
         h = _c_void_p()
         check(lib.latentmoe_create(ctypes.byref(self.dims), k, self.flags, ctypes.byref(h)),
               "latentmoe_create")
@@ -247,6 +261,38 @@ class LatentMoE:
               "latentmoe_get_stage_times")
         return {stage_name(i): buf[i] for i in range(n)}
 
+    def fp8_state(self):
+        """{"scales": [s_z, s_h] for the next forward, "last_amax": the last
+        forward's maxima, "steps": forwards entered into the history}."""
+        sc = (ctypes.c_float * FP8_TENSORS)()
+        am = (ctypes.c_float * FP8_TENSORS)()
+        st = _i64(0)
+        check(load().latentmoe_get_fp8_state(self.handle, sc, am, ctypes.byref(st)),
+              "latentmoe_get_fp8_state")
+        return {"scales": list(sc), "last_amax": list(am), "steps": st.value}
+
+    def fp8_codes(self, T: int, device, stream=None):
+        """(z codes [T*k, l], h codes [T*k, F]) uint8 of the last forward."""
+        import torch
+        S = T * self.k
+        zc = torch.empty((S, self.dims.latent), dtype=torch.uint8, device=device)
+        hc = torch.empty((S, self.dims.ffn), dtype=torch.uint8, device=device)
+        check(load().latentmoe_get_fp8_codes(self.handle, zc.data_ptr(), hc.data_ptr(),
+                                             _stream(stream)), "latentmoe_get_fp8_codes")
+        return zc, hc
+
+    def set_fp8_scales(self, scales) -> None:
+        sc = (ctypes.c_float * FP8_TENSORS)(*scales)
+        check(load().latentmoe_set_fp8_scales(self.handle, sc), "latentmoe_set_fp8_scales")
+
+    def fp8_weight_scales(self):
+        """[3, E] list of lists: scales of W_g, W_u, W_d per expert."""
+        E = self.dims.num_experts
+        buf = (ctypes.c_float * (3 * E))()
+        check(load().latentmoe_get_fp8_weight_scales(self.handle, buf),
+              "latentmoe_get_fp8_weight_scales")
+        return [list(buf[m * E:(m + 1) * E]) for m in range(3)]
+
     def launch_count(self) -> int:
         v = _i64(0)
         check(load().latentmoe_get_launch_count(self.handle, ctypes.byref(v)),
@@ -268,6 +314,20 @@ def debug_grouped_gemm(A, B, C, offsets, groups: int, M: int, N: int, K: int, mo
     return load().latentmoe_debug_grouped_gemm(A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                                offsets.data_ptr(), groups, M, N, K, mode,
                                                _stream(stream))
+
+
+def quantize_e4m3(src, codes, scales, stream=None) -> int:
+    """src bf16 [G, R, C] (device) -> codes uint8 [G, R, C], scales fp32 [G]."""
+    G, R, C = src.shape
+    return load().latentmoe_quantize_e4m3(src.data_ptr(), G, R, C, codes.data_ptr(),
+                                          scales.data_ptr(), _stream(stream))
+
+
+def debug_grouped_gemm_e4m3(A, B, scales, C, amax, offsets, groups: int, M: int, N: int, K: int,
+                            mode: int, stream=None) -> int:
+    return load().latentmoe_debug_grouped_gemm_e4m3(
+        A.data_ptr(), B.data_ptr(), scales.data_ptr(), C.data_ptr(), _ptr(amax),
+        offsets.data_ptr(), groups, M, N, K, mode, _stream(stream))
 
 
 def debug_status() -> int:

@@ -17,8 +17,15 @@
 //   6 combine         c[t] = sum_j g[t,j] o[pos[t,j]]        gather, fp32
 //   7 shared_gate_up  s = SiLU(x W_gs^T) * (x W_us^T)        tcgen05 (F_s > 0)
 //   8 up_proj         y = c W_up^T (+ s W_ds^T)              tcgen05, dual-K
+//   9 fp8_scales      (E4M3 experts only) delayed-scaling update of the
+//                     scales of z and h                      1 small kernel
+//
+// With LATENTMOE_FP8_EXPERTS the expert GEMMs (4, 5) take E4M3 operands:
+// down_proj writes z as E4M3 codes, expert_gate_up writes h as E4M3 codes,
+// and both record their maxima for the scale update.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -33,10 +40,11 @@ using lmoe::GemmMaps;
 
 namespace {
 
-constexpr int kNumStages = 9;
+constexpr int kNumStages = 10;
 const char* const kStageNames[kNumStages] = {
     "router",      "replay_gates", "sort",           "down_proj", "expert_gate_up",
-    "expert_down", "combine",      "shared_gate_up", "up_proj"};
+    "expert_down", "combine",      "shared_gate_up", "up_proj",   "fp8_scales"};
+constexpr int kFp8Acts = 2;  // scaled activations: 0 = z, 1 = h
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -73,24 +81,42 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Token rows for the grouped kernel: boxes of kGTokBox rows x kGBK columns.
-bool make_token_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols) {
+// 2-D byte tensor (E4M3 codes) [rows, cols] read in boxes of 128 columns x
+// box_rows rows with 128-byte swizzle.
+bool make_map_u8(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                 uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token rows for the grouped kernel: boxes of kGTokBox rows x 128 bytes
+// (kGBK bf16 or kGBK8 E4M3 columns).
+bool make_token_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                    bool f8 = false) {
+  if (f8) return make_map_u8(map, ptr, rows, cols, cols, lmoe::kGTokBox);
   return make_map(map, ptr, rows, cols, cols, lmoe::kGTokBox, lmoe::kGBK);
 }
 
 // Packed weight tiles (see pack.cu): `tiles` contiguous blocks of 128 rows x
-// kGBK bf16, read one whole tile per box with the grouped kernel's swizzle.
-bool make_tile_map(CUtensorMap* map, const void* ptr, uint64_t tiles) {
+// 128 bytes, read one whole tile per box with the grouped kernel's swizzle.
+bool make_tile_map(CUtensorMap* map, const void* ptr, uint64_t tiles, bool f8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || ptr == nullptr || tiles == 0) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(lmoe::kGBK), 128, tiles};
-  const cuuint64_t strides[2] = {lmoe::kGBK * 2, 128 * lmoe::kGBK * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(lmoe::kGBK), 128, 1};
+  const cuuint64_t cols = f8 ? lmoe::kGBK8 : lmoe::kGBK;
+  const cuuint64_t dims[3] = {cols, 128, tiles};
+  const cuuint64_t strides[2] = {128, 128 * 128};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(cols), 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw =
-      lmoe::kGBK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -118,7 +144,10 @@ struct latentmoe {
   int device = 0;
   int sms = 1;
   bool loaded = false;
+  bool fp8 = false;             // E4M3 expert GEMMs
   latentmoe_weights w;          // the library-owned copies below
+  float* w_scale = nullptr;     // E4M3: [3E] scales of W_g, W_u, W_d per expert (in wmem)
+  lmoe::Fp8State* f8 = nullptr; // E4M3: delayed-scaling state (in ws)
   void* wmem = nullptr;          // one allocation holding every weight copy
   GemmMaps m_router, m_down, m_shared, m_up;
   CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
@@ -239,7 +268,8 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   if (dims == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   const latentmoe_dims d = *dims;
   if (flags & ~static_cast<uint32_t>(LATENTMOE_RENORM | LATENTMOE_ROUTER_BIAS |
-                                     LATENTMOE_OUT_FP32 | LATENTMOE_SELECT_BIAS))
+                                     LATENTMOE_OUT_FP32 | LATENTMOE_SELECT_BIAS |
+                                     LATENTMOE_FP8_EXPERTS))
     return LATENTMOE_ERR_INVALID_ARG;
   if ((flags & LATENTMOE_ROUTER_BIAS) && (flags & LATENTMOE_SELECT_BIAS))
     return LATENTMOE_ERR_INVALID_ARG;
@@ -263,6 +293,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->dims = d;
   h->k = top_k;
   h->flags = flags;
+  h->fp8 = (flags & LATENTMOE_FP8_EXPERTS) != 0;
   memset(&h->w, 0, sizeof(h->w));
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) {
@@ -290,6 +321,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   const size_t o_zp = take(S * l * 2), o_h = take(S * F * 2), o_o = take(S * l * 2);
   const size_t o_c = take(T * l * 2), o_sh = take(Fs > 0 ? T * Fs * 2 : 16);
   const size_t o_status = take(16);
+  const size_t o_f8 = take(sizeof(lmoe::Fp8State));
   e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -313,7 +345,15 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->cb = reinterpret_cast<__nv_bfloat16*>(base + o_c);
   h->sh = reinterpret_cast<__nv_bfloat16*>(base + o_sh);
   h->status = reinterpret_cast<unsigned*>(base + o_status);
+  h->f8 = reinterpret_cast<lmoe::Fp8State*>(base + o_f8);
   e = cudaMemset(h->status, 0, 16);
+  if (e == cudaSuccess) {
+    // delayed scaling starts with an empty history and unit scales
+    lmoe::Fp8State init;
+    memset(&init, 0, sizeof(init));
+    for (int i = 0; i < lmoe::kFp8Tensors; ++i) init.scale[i] = 1.0f;
+    e = cudaMemcpy(h->f8, &init, sizeof(init), cudaMemcpyHostToDevice);
+  }
   if (e != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -361,7 +401,10 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   };
   const size_t o_r = take(E * dd * 2), o_b = take(bias ? E * 4 : 16), o_dn = take(l * dd * 2);
   const size_t o_up = take(dd * l * 2);
-  const size_t o_g = take(E * F * l * 2), o_u = take(E * F * l * 2), o_d = take(E * l * F * 2);
+  // expert weights: packed bf16 tiles, or packed E4M3 codes plus their scales
+  const uint64_t eb = h->fp8 ? 1 : 2;
+  const size_t o_g = take(E * F * l * eb), o_u = take(E * F * l * eb), o_d = take(E * l * F * eb);
+  const size_t o_ws = take(h->fp8 ? 3 * E * 4 : 16), o_wa = take(h->fp8 ? 3 * E * 4 : 16);
   const size_t o_gs = take(shared ? Fs * dd * 2 : 16), o_us = take(shared ? Fs * dd * 2 : 16);
   const size_t o_ds = take(shared ? dd * Fs * 2 : 16);
   // the caller's writes to its weights may still be in flight on any stream
@@ -394,6 +437,7 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
     o.w_us = base + o_us;
     o.w_ds = base + o_ds;
   }
+  h->w_scale = h->fp8 ? reinterpret_cast<float*>(base + o_ws) : nullptr;
   const auto dd2d = cudaMemcpyDeviceToDevice;
   LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_r), w->w_r, E * dd * 2, dd2d));
   if (bias) LMOE_CK(h, cudaMemcpy(const_cast<float*>(o.b_r), w->b_r, E * 4, dd2d));
@@ -405,22 +449,40 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
     LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_ds), w->w_ds, dd * Fs * 2, dd2d));
   }
   typedef const __nv_bfloat16* cbf;
-  typedef __nv_bfloat16* mbf;
-  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_g), const_cast<mbf>(static_cast<cbf>(o.w_g)),
-                                     static_cast<long long>(E * F), static_cast<int>(l), h->sms, 0));
-  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_u), const_cast<mbf>(static_cast<cbf>(o.w_u)),
-                                     static_cast<long long>(E * F), static_cast<int>(l), h->sms, 0));
-  LMOE_CK(h, lmoe::launch_pack_tiles(static_cast<cbf>(w->w_d), const_cast<mbf>(static_cast<cbf>(o.w_d)),
-                                     static_cast<long long>(E * l), static_cast<int>(F), h->sms, 0));
+  const void* srcs[3] = {w->w_g, w->w_u, w->w_d};
+  void* dsts[3] = {const_cast<void*>(o.w_g), const_cast<void*>(o.w_u), const_cast<void*>(o.w_d)};
+  const long long mrows[3] = {static_cast<long long>(F), static_cast<long long>(F),
+                              static_cast<long long>(l)};
+  const long long mcols[3] = {static_cast<long long>(l), static_cast<long long>(l),
+                              static_cast<long long>(F)};
+  if (h->fp8) {
+    // s = max |W_e| / 448 per expert matrix, then codes in the packed layout
+    unsigned* amax = reinterpret_cast<unsigned*>(base + o_wa);
+    LMOE_CK(h, cudaMemset(amax, 0, 3 * E * 4));
+    for (int m = 0; m < 3; ++m)
+      LMOE_CK(h, lmoe::launch_absmax_groups(static_cast<cbf>(srcs[m]), static_cast<long long>(E),
+                                            mrows[m] * mcols[m], amax + m * E, h->sms, 0));
+    LMOE_CK(h, lmoe::launch_scales_from_amax(amax, static_cast<int>(3 * E), h->w_scale, 0));
+    for (int m = 0; m < 3; ++m)
+      LMOE_CK(h, lmoe::launch_quantize_e4m3(static_cast<cbf>(srcs[m]),
+                                            static_cast<uint8_t*>(dsts[m]),
+                                            static_cast<long long>(E) * mrows[m], mcols[m],
+                                            mrows[m], h->w_scale + m * E, true, h->sms, 0));
+  } else {
+    for (int m = 0; m < 3; ++m)
+      LMOE_CK(h, lmoe::launch_pack_tiles(srcs[m], dsts[m], static_cast<long long>(E) * mrows[m],
+                                         mcols[m] * 2, h->sms, 0));
+  }
   LMOE_CK(h, cudaDeviceSynchronize());
 
   bool ok = true;
   ok &= make_map(&h->m_router.b, o.w_r, E, dd, dd, 256);
   ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);
   ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
-  ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l / lmoe::kGBK));
-  ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l / lmoe::kGBK));
-  ok &= make_tile_map(&h->m_wd, o.w_d, E * l / 128 * (F / lmoe::kGBK));
+  // tiles of 128 rows x 128 bytes
+  ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l * eb / 128), h->fp8);
+  ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l * eb / 128), h->fp8);
+  ok &= make_tile_map(&h->m_wd, o.w_d, E * l / 128 * (F * eb / 128), h->fp8);
   ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 256);
   if (shared) {
     ok &= make_map(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
@@ -460,8 +522,8 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   CUtensorMap mx, mx32, mzp, mh, mc, msh;
   bool ok = make_map(&mx, x, T, dd, dd, 128);
   ok &= make_map(&mx32, x, T, dd, dd, 128, lmoe::kRBK);
-  ok &= make_token_map(&mzp, h->zp, S, l);
-  ok &= make_token_map(&mh, h->hb, S, F);
+  ok &= make_token_map(&mzp, h->zp, S, l, h->fp8);
+  ok &= make_token_map(&mh, h->hb, S, F, h->fp8);
   ok &= make_map(&mc, h->cb, T, l, l, 128);
   if (Fs > 0) ok &= make_map(&msh, h->sh, T, Fs, Fs, 128);
   if (!ok) return LATENTMOE_ERR_CUDA;
@@ -525,7 +587,13 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.ldo = l;
     a.pos = h->pos;
     a.topk = k;
-    LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    if (h->fp8) {
+      a.out_scale = &h->f8->scale[0];
+      a.out_amax = &h->f8->amax[0];
+      LMOE_CK(h, lmoe::launch_gemm_scatter_f8(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    } else {
+      LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    }
     h->launches += 1;
   }
   record(h, slot_base, 4, s);
@@ -536,13 +604,21 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.num_groups = E;
     a.seg_offsets = h->offsets;
     a.fblocks = F / 128;
-    a.kb = l / lmoe::kGBK;
+    a.kb = l / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
     a.w_group_rows = F;
     a.n_out = F;
     a.out = h->hb;
     a.ldo = F;
     a.status = h->status;
-    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, mzp, h->m_wg, h->m_wu, a, h->sms, s));
+    if (h->fp8) {
+      a.w_scale0 = h->w_scale;
+      a.w_scale1 = h->w_scale + E;
+      a.in_scale = &h->f8->scale[0];
+      a.out_scale = &h->f8->scale[1];
+      a.out_amax = &h->f8->amax[1];
+    }
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu, a,
+                                         h->sms, s));
     h->launches += 1;
   }
   record(h, slot_base, 5, s);
@@ -553,13 +629,18 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.num_groups = E;
     a.seg_offsets = h->offsets;
     a.fblocks = ceil_div(l, 256);
-    a.kb = F / lmoe::kGBK;
+    a.kb = F / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
     a.w_group_rows = l;
     a.n_out = l;
     a.out = h->ob;
     a.ldo = l;
     a.status = h->status;
-    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, mh, h->m_wd, h->m_wd, a, h->sms, s));
+    if (h->fp8) {
+      a.w_scale0 = a.w_scale1 = h->w_scale + 2 * E;
+      a.in_scale = &h->f8->scale[1];
+    }
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd, a,
+                                         h->sms, s));
     h->launches += 1;
   }
   record(h, slot_base, 6, s);
@@ -603,6 +684,12 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 9, s);
+  // 9: delayed scaling: this forward's maxima enter the history, next scales
+  if (h->fp8) {
+    LMOE_CK(h, lmoe::launch_fp8_update(h->f8, kFp8Acts, s));
+    h->launches += 1;
+  }
+  record(h, slot_base, 10, s);
   h->last_T = T;
   return LATENTMOE_OK;
 }
@@ -769,6 +856,85 @@ int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches) {
 
 int latentmoe_last_cuda_error(latentmoe_t h) { return h ? h->last_cuda : 0; }
 
+// ---------------------------------------------------------------- E4M3
+int latentmoe_get_fp8_state(latentmoe_t h, float* scales, float* last_amax, int64_t* steps) {
+  if (h == nullptr || scales == nullptr || last_amax == nullptr || steps == nullptr)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->fp8) return LATENTMOE_ERR_UNSUPPORTED;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  lmoe::Fp8State st;
+  LMOE_CK(h, cudaMemcpy(&st, h->f8, offsetof(lmoe::Fp8State, hist), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < kFp8Acts; ++i) {
+    scales[i] = st.scale[i];
+    last_amax[i] = st.last_amax[i];
+  }
+  *steps = st.steps;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_fp8_codes(latentmoe_t h, uint8_t* z_codes, uint8_t* h_codes,
+                            latentmoe_stream_t st) {
+  if (h == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->fp8) return LATENTMOE_ERR_UNSUPPORTED;
+  if (h->last_T < 1) return LATENTMOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const size_t S = static_cast<size_t>(h->last_T) * h->k;
+  if (z_codes)
+    LMOE_CK(h, cudaMemcpyAsync(z_codes, h->zp, S * h->dims.latent, cudaMemcpyDeviceToDevice, s));
+  if (h_codes)
+    LMOE_CK(h, cudaMemcpyAsync(h_codes, h->hb, S * h->dims.ffn, cudaMemcpyDeviceToDevice, s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_set_fp8_scales(latentmoe_t h, const float* scales) {
+  if (h == nullptr || scales == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->fp8) return LATENTMOE_ERR_UNSUPPORTED;
+  for (int i = 0; i < kFp8Acts; ++i)
+    if (!(scales[i] > 0.0f) || !(scales[i] < 3.0e38f)) return LATENTMOE_ERR_INVALID_ARG;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  lmoe::Fp8State init;
+  memset(&init, 0, sizeof(init));
+  for (int i = 0; i < lmoe::kFp8Tensors; ++i) init.scale[i] = i < kFp8Acts ? scales[i] : 1.0f;
+  LMOE_CK(h, cudaMemcpy(h->f8, &init, sizeof(init), cudaMemcpyHostToDevice));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_fp8_weight_scales(latentmoe_t h, float* scales) {
+  if (h == nullptr || scales == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->fp8) return LATENTMOE_ERR_UNSUPPORTED;
+  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  LMOE_CK(h, cudaMemcpy(scales, h->w_scale, 3 * h->dims.num_experts * 4, cudaMemcpyDeviceToHost));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_quantize_e4m3(const void* src, int64_t groups, int64_t rows, int64_t cols,
+                            uint8_t* codes, float* scales, latentmoe_stream_t st) {
+  if (src == nullptr || codes == nullptr || scales == nullptr || groups < 1 || rows < 1 ||
+      cols < 1)
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (cols % 16 || groups > 65535 || !aligned16(src) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return LATENTMOE_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  const int sms = num_sms();
+  // the scale buffer first holds the maxima (float bits), then the scales
+  unsigned* amax = reinterpret_cast<unsigned*>(scales);
+  if (cudaMemsetAsync(amax, 0, groups * 4, s) != cudaSuccess) return LATENTMOE_ERR_CUDA;
+  typedef const __nv_bfloat16* cbf;
+  if (lmoe::launch_absmax_groups(static_cast<cbf>(src), groups, rows * cols, amax, sms, s) !=
+          cudaSuccess ||
+      lmoe::launch_scales_from_amax(amax, static_cast<int>(groups), scales, s) != cudaSuccess ||
+      lmoe::launch_quantize_e4m3(static_cast<cbf>(src), codes, groups * rows, cols, rows, scales,
+                                 false, sms, s) != cudaSuccess)
+    return LATENTMOE_ERR_CUDA;
+  return LATENTMOE_OK;
+}
+
 // ---------------------------------------------------------------- debug GEMM
 int latentmoe_debug_status(uint32_t* device_status);
 
@@ -801,8 +967,7 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
       cudaGetLastError();
       return LATENTMOE_ERR_OUT_OF_MEMORY;
     }
-    if (lmoe::launch_pack_tiles(static_cast<const __nv_bfloat16*>(B), bp, brows,
-                                static_cast<int>(K), num_sms(), s) != cudaSuccess) {
+    if (lmoe::launch_pack_tiles(B, bp, brows, K * 2, num_sms(), s) != cudaSuccess) {
       cudaFree(bp);
       return LATENTMOE_ERR_CUDA;
     }
@@ -830,7 +995,7 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
     ga.ldo = N;
     ga.status = status;
     cudaError_t e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain,
-                                              tok, w0, w1, ga, num_sms(), s);
+                                              false, tok, w0, w1, ga, num_sms(), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(bp);
     return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
@@ -883,6 +1048,66 @@ int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C, const in
   if (offsets == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   return debug_gemm_impl(A, B, C, offsets, groups, M, N, K, mode,
                          reinterpret_cast<cudaStream_t>(st));
+}
+
+int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B, const float* scales,
+                                      void* C, uint32_t* amax, const int32_t* offsets,
+                                      int64_t G, int64_t M, int64_t N, int64_t K, int mode,
+                                      latentmoe_stream_t st) {
+  if (!A || !B || !scales || !C || !offsets || M < 1 || N < 1 || K < 1 || G < 1 ||
+      (mode != 1 && mode != 2) || (mode == 2 && amax == nullptr))
+    return LATENTMOE_ERR_INVALID_ARG;
+  if (K % 128 || N % 128 || M > (1 << 30) || N > (1 << 20) || G > lmoe::kMaxGroups)
+    return LATENTMOE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return LATENTMOE_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  unsigned* status = debug_status_word();
+  if (status == nullptr) return LATENTMOE_ERR_CUDA;
+  const long long brows = G * N * (mode == 2 ? 2 : 1);
+  uint8_t* bp = nullptr;
+  if (cudaMalloc(&bp, brows * K) != cudaSuccess) {
+    cudaGetLastError();
+    return LATENTMOE_ERR_OUT_OF_MEMORY;
+  }
+  if (lmoe::launch_pack_tiles(B, bp, brows, K, num_sms(), s) != cudaSuccess) {
+    cudaFree(bp);
+    return LATENTMOE_ERR_CUDA;
+  }
+  const uint64_t tiles_half = static_cast<uint64_t>(G * N / 128 * (K / 128));
+  CUtensorMap tok, w0, w1;
+  bool ok = make_token_map(&tok, A, M, K, true);
+  ok &= make_tile_map(&w0, bp, tiles_half, true);
+  if (mode == 2)
+    ok &= make_tile_map(&w1, bp + G * N * K, tiles_half, true);
+  else
+    w1 = w0;
+  if (!ok) {
+    cudaFree(bp);
+    return LATENTMOE_ERR_CUDA;
+  }
+  lmoe::GroupedArgs ga;
+  memset(&ga, 0, sizeof(ga));
+  ga.num_groups = static_cast<int>(G);
+  ga.seg_offsets = offsets;
+  ga.fblocks = mode == 2 ? static_cast<int>(N / 128) : ceil_div(N, 256);
+  ga.kb = static_cast<int>(K / lmoe::kGBK8);
+  ga.w_group_rows = static_cast<int>(N);
+  ga.n_out = static_cast<int>(N);
+  ga.out = C;
+  ga.ldo = N;
+  ga.status = status;
+  ga.in_scale = scales;
+  ga.out_scale = scales + 1;
+  ga.w_scale0 = scales + 2;
+  ga.w_scale1 = mode == 2 ? scales + 2 + G : scales + 2;
+  ga.out_amax = amax;
+  cudaError_t e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, true,
+                                            tok, w0, w1, ga, num_sms(), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  cudaFree(bp);
+  return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
 }
 
 namespace {

@@ -24,17 +24,20 @@
 //   kEpiSwiglu   B holds 128 gate rows then 128 up rows of the same output
 //                features; C[row, f] = bf16(SiLU(gate) * up)
 //   kEpiScatter  token row t is written to rows pos[t*k + j], j < k, of C
+//   kEpiScatterF8  the same with C as E4M3 codes of acc / out_scale, and the
+//                running max |acc| of the valid rows recorded in out_amax
 //
 // Ragged edges: rows past a segment or past M are computed on whatever TMA
 // brought in (zeros past the tensor) and never stored; columns past N are not
 // stored either.
 #pragma once
 
+#include "fp8.cuh"
 #include "ptx.cuh"
 
 namespace lmoe {
 
-enum EpiMode : int { kEpiBf16 = 0, kEpiF32 = 1, kEpiSwiglu = 2, kEpiScatter = 3 };
+enum EpiMode : int { kEpiBf16 = 0, kEpiF32 = 1, kEpiSwiglu = 2, kEpiScatter = 3, kEpiScatterF8 = 4 };
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
@@ -73,6 +76,8 @@ struct GemmArgs {
   int topk;
   unsigned* status;        // device status word
   int hints;               // bit 0: A tiles evict_last in L2; bit 1: B tiles evict_first
+  const float* out_scale;  // kEpiScatterF8: [1] scale the output is quantized with
+  unsigned* out_amax;      // kEpiScatterF8: [1] running max |acc| (float bits)
 };
 
 struct TileCoord {
@@ -159,6 +164,49 @@ __device__ __forceinline__ void store_chunk_bf16_staged(const GemmArgs& a,
       } else {
         *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * a.ldo + col +
                                   piece * 8) = w;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// E4M3 output of one 32-column chunk, scattered like kEpiScatter: each lane
+// quantizes its row to 32 bytes, the warp stages them (16-byte pieces
+// XOR-swizzled by row / 4, conflict-free both ways) and writes 16 rows per
+// instruction, 2 lanes per row.
+__device__ __forceinline__ void store_chunk_f8_scatter(const GemmArgs& a, const uint32_t (&v)[32],
+                                                       float inv, uint8_t* stage,
+                                                       long long warp_row0, int rows_valid,
+                                                       int col) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    uint4 w;
+    const int b = 16 * p;
+    w.x = quant4_e4m3(__uint_as_float(v[b + 0]), __uint_as_float(v[b + 1]),
+                      __uint_as_float(v[b + 2]), __uint_as_float(v[b + 3]), inv);
+    w.y = quant4_e4m3(__uint_as_float(v[b + 4]), __uint_as_float(v[b + 5]),
+                      __uint_as_float(v[b + 6]), __uint_as_float(v[b + 7]), inv);
+    w.z = quant4_e4m3(__uint_as_float(v[b + 8]), __uint_as_float(v[b + 9]),
+                      __uint_as_float(v[b + 10]), __uint_as_float(v[b + 11]), inv);
+    w.w = quant4_e4m3(__uint_as_float(v[b + 12]), __uint_as_float(v[b + 13]),
+                      __uint_as_float(v[b + 14]), __uint_as_float(v[b + 15]), inv);
+    *reinterpret_cast<uint4*>(stage + lane * 32 + ((p ^ ((lane >> 2) & 1)) * 16)) = w;
+  }
+  __syncwarp();
+  const int piece = lane & 1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rr = h * 16 + (lane >> 1);
+    const uint4 w =
+        *reinterpret_cast<const uint4*>(stage + rr * 32 + ((piece ^ ((rr >> 2) & 1)) * 16));
+    if (rr < rows_valid) {
+      const long long row = warp_row0 + rr;
+      for (int j = 0; j < a.topk; ++j) {
+        const int dst_row = a.pos[row * a.topk + j];
+        if (dst_row < 0) continue;
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                  static_cast<long long>(dst_row) * a.ldo + col + piece * 16) = w;
       }
     }
   }
@@ -400,6 +448,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* stage_w = stage_smem + (warp - 2) * kStageWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
+    const float out_inv = MODE == kEpiScatterF8 ? inv_scale(*a.out_scale) : 1.0f;
+    float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const TileCoord c = decode_tile(t, a, seg_s, mt_s, kBRowsPerTile);
       if (!warp_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, a.status)) break;
@@ -434,6 +484,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int col = c.n * kBN + ch * 32;
           if constexpr (MODE == kEpiF32) {
             if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
+          } else if constexpr (MODE == kEpiScatterF8) {
+            if (col < a.N) {
+              if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(v[i])));
+              }
+              store_chunk_f8_scatter(a, v, out_inv, stage_w, warp_row0, warp_rows, col);
+            }
           } else {
             if (col < a.N) store_chunk_bf16_staged<MODE>(a, v, stage_w, warp_row0, warp_rows, col);
           }
@@ -445,6 +503,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    if constexpr (MODE == kEpiScatterF8) {
+      amax = warp_max(amax);
+      if (lane == 0) atomic_max_nonneg(a.out_amax, amax);
     }
   }
 

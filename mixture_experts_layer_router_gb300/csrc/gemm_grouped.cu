@@ -1,29 +1,34 @@
-// Grouped expert GEMMs (weights on the M side): SwiGLU gate+up and plain down.
+// Grouped expert GEMMs (weights on the M side): SwiGLU gate+up and plain
+// down, with bf16 or E4M3 operands.
 #include "gemm_grouped.cuh"
 #include "kernels.h"
 
 namespace lmoe {
 
-template <int MODE>
+template <int MODE, bool F8>
 static cudaError_t launch_grouped_impl(const CUtensorMap& tok, const CUtensorMap& w0,
                                        const CUtensorMap& w1, const GroupedArgs& a, int grid,
                                        cudaStream_t s) {
   static bool smem_set = false;
   if (!smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gemm_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
+    const cudaError_t e = cudaFuncSetAttribute(gemm_grouped_kernel<MODE, F8>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kGSmemBytes);
     if (e != cudaSuccess) return e;
     smem_set = true;
   }
-  gemm_grouped_kernel<MODE><<<grid, kGThreads, kGSmemBytes, s>>>(tok, w0, w1, a);
+  gemm_grouped_kernel<MODE, F8><<<grid, kGThreads, kGSmemBytes, s>>>(tok, w0, w1, a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_grouped(int mode, const CUtensorMap& tok, const CUtensorMap& w0,
+cudaError_t launch_gemm_grouped(int mode, bool f8, const CUtensorMap& tok, const CUtensorMap& w0,
                                 const CUtensorMap& w1, const GroupedArgs& a, int grid,
                                 cudaStream_t s) {
-  return mode == kGrpSwiglu ? launch_grouped_impl<kGrpSwiglu>(tok, w0, w1, a, grid, s)
-                            : launch_grouped_impl<kGrpPlain>(tok, w0, w1, a, grid, s);
+  if (f8)
+    return mode == kGrpSwiglu ? launch_grouped_impl<kGrpSwiglu, true>(tok, w0, w1, a, grid, s)
+                              : launch_grouped_impl<kGrpPlain, true>(tok, w0, w1, a, grid, s);
+  return mode == kGrpSwiglu ? launch_grouped_impl<kGrpSwiglu, false>(tok, w0, w1, a, grid, s)
+                            : launch_grouped_impl<kGrpPlain, false>(tok, w0, w1, a, grid, s);
 }
 
 }  // namespace lmoe

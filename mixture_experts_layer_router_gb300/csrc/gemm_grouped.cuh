@@ -32,8 +32,18 @@
 // Tiles are enumerated on the device from the segment offsets: expert-major,
 // then feature block, then token chunk, so chunks of one feature block run
 // on neighbouring CTAs at the same time and share the weight tile in L2.
+//
+// E4M3 variant (F8 = true): weights and token rows are FP8 codes, a k-block
+// is 128 elements (still one 128-byte swizzle row, so tiles, stages and
+// descriptors are byte-for-byte the same) and the MMA is kind::f8f6f4 with
+// K = 32 per instruction. The epilogue multiplies the accumulators by the
+// token scale times the group's weight scale; the SwiGLU epilogue then
+// records max |h| and writes h as E4M3 codes with the scale given for it
+// ("The Training and RL Infrastructure Behind MAI-Thinking-1", section
+// "2. Numerics": FP8 forward GEMMs with delayed scaling).
 #pragma once
 
+#include "fp8.cuh"
 #include "ptx.cuh"
 
 namespace lmoe {
@@ -41,6 +51,7 @@ namespace lmoe {
 enum GroupedMode : int { kGrpSwiglu = 0, kGrpPlain = 1 };
 
 constexpr int kGBK = 64;                      // one 128-byte swizzle row
+constexpr int kGBK8 = 128;                    // E4M3: one 128-byte swizzle row
 constexpr int kGStages = 3;
 constexpr int kGWeightTile = 128 * kGBK * 2;  // 16 KB
 constexpr int kGTokenTile = 256 * kGBK * 2;   // 32 KB
@@ -64,12 +75,19 @@ struct GroupedArgs {
   int kb;                  // k-blocks (K / 64)
   int w_group_rows;        // weight rows per group in the weight maps
   int n_out;               // output features (columns of out)
-  void* out;               // bf16 [rows, n_out], rows in slot order
+  void* out;               // bf16 [rows, n_out] (E4M3 SwiGLU: codes), rows in slot order
   long long ldo;
   unsigned* status;
+  // E4M3 variant only
+  const float* w_scale0;   // [G] scale of the weights of accumulator 0, per group
+  const float* w_scale1;   // [G] accumulator 1 (SwiGLU: the up rows)
+  const float* in_scale;   // [1] scale of the token rows
+  const float* out_scale;  // [1] SwiGLU: scale h is quantized with
+  unsigned* out_amax;      // [1] SwiGLU: running max |h| (float bits)
 };
 
 struct GTile {
+  int g;      // group
   int tok0;   // first token row
   int len;    // valid tokens (<= 256)
   int n;      // MMA N: len rounded up to 16
@@ -99,6 +117,7 @@ __device__ __forceinline__ GTile decode_gtile(int t, const GroupedArgs& a, const
   const int f = local / nch;
   const int c = local - f * nch;
   GTile r;
+  r.g = g;
   r.tok0 = seg_s[g] + c * cs;
   r.len = min(cs, n - c * cs);
   r.n = (r.len + 15) & ~15;
@@ -140,7 +159,34 @@ __device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_
   __syncwarp();
 }
 
-template <int MODE>
+// E4M3 form of gstore_chunk: lane `lane` holds the codes of its feature for
+// 32 tokens (token 4j+b in byte b of q[j]). Each token row segment is 32
+// bytes; pieces are XOR-swizzled by (row / 4) so that both the byte writes
+// and the 16-byte reads are free of bank conflicts.
+__device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint32_t (&q)[8],
+                                                uint8_t* stage, long long tok_row0,
+                                                int tok_valid, int feat0) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int sw = ((lane >> 4) ^ ((j >> 2) & 1)) * 16 + (lane & 15);
+    stage[j * 32 + sw] = static_cast<uint8_t>(q[j >> 2] >> (8 * (j & 3)));
+  }
+  __syncwarp();
+  const int piece = lane & 1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rr = h * 16 + (lane >> 1);
+    const uint4 w =
+        *reinterpret_cast<const uint4*>(stage + rr * 32 + ((piece ^ ((rr >> 2) & 1)) * 16));
+    if (rr < tok_valid)
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (tok_row0 + rr) * a.ldo + feat0 +
+                                piece * 16) = w;
+  }
+  __syncwarp();
+}
+
+template <int MODE, bool F8>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_grouped_kernel(const __grid_constant__ CUtensorMap tmTok,
                         const __grid_constant__ CUtensorMap tmW0,
@@ -251,8 +297,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
               tma_load_3d(&tmW0, &full_bar[stage], sw1, 0, 0, (rt0 + 1) * a.kb + kb, pol_w);
           }
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(&tmTok, &full_bar[stage], stok + b * kGTokBoxBytes, kb * kGBK,
-                        c.tok0 + b * kGTokBox, pol_t);
+            tma_load_2d(&tmTok, &full_bar[stage], stok + b * kGTokBoxBytes,
+                        kb * (F8 ? kGBK8 : kGBK), c.tok0 + b * kGTokBox, pol_t);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kGStages) {
@@ -274,7 +320,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
         const bool two = second_acc_used<MODE>(a, c.f);
-        const uint32_t idesc = instr_desc_bf16(128, c.n);
+        const uint32_t idesc = F8 ? instr_desc_e4m3(128, c.n) : instr_desc_bf16(128, c.n);
         if (!wait_bounded(tempty_bar, acc_phase ^ 1u, abort_flag, a.status)) break;
         tc_fence_after_sync();
         for (int kb = 0; kb < a.kb; ++kb) {
@@ -287,11 +333,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint64_t d0 = smem_desc_sw128(sw0);
           const uint64_t d1 = smem_desc_sw128(sw0 + kGWeightTile);
           const uint64_t dt = smem_desc_sw128(sw0 + 2 * kGWeightTile);
+          // 4 instructions per 128-byte row, each 32 bytes of K (+2 in addr >> 4)
 #pragma unroll
-          for (int k = 0; k < kGBK / 16; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            tc_mma(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
-            if (two) tc_mma(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            if constexpr (F8) {
+              tc_mma_f8(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+              if (two) tc_mma_f8(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            } else {
+              tc_mma(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+              if (two) tc_mma(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            }
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == kGStages) {
@@ -313,13 +365,52 @@ __global__ void __launch_bounds__(kGThreads, 1)
     uint8_t* stage_w = stage_smem + (warp - 2) * kGStageWarpBytes;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc_phase = 0;
+    const float in_s = F8 ? *a.in_scale : 1.0f;
+    const float out_inv = (F8 && MODE == kGrpSwiglu) ? inv_scale(*a.out_scale) : 1.0f;
+    float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
       const bool two = second_acc_used<MODE>(a, c.f);
       if (!warp_wait_bounded(tfull_bar, acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
       const int nchunks = (c.len + 31) / 32;
-      if constexpr (MODE == kGrpSwiglu) {
+      if constexpr (MODE == kGrpSwiglu && F8) {
+        // h = SiLU(s0 acc0) * (s1 acc1), its maximum over the valid tokens,
+        // and its E4M3 codes; TMEM goes back to the MMA before the stores
+        const float sg = in_s * a.w_scale0[c.g], su = in_s * a.w_scale1[c.g];
+        uint32_t hq[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = half + 2 * i;
+          if (ch < nchunks) {
+            uint32_t g[32], u[32];
+            tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
+            tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
+            tmem_ld_wait();
+            const int valid = c.len - ch * 32;
+            float hv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              hv[j] = silu(__uint_as_float(g[j]) * sg) * (__uint_as_float(u[j]) * su);
+              if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              hq[i][j] = quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3],
+                                     out_inv);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(tempty_bar);
+        const int feat0 = c.f * 128 + quarter * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = half + 2 * i;
+          if (ch < nchunks)
+            gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+                            c.len - ch * 32, feat0);
+        }
+      } else if constexpr (MODE == kGrpSwiglu) {
         // Read both accumulators and form h = SiLU(gate) * up for this
         // warp's chunks (at most 4), packed to bf16 in registers; then hand
         // TMEM back to the MMA before the slower transposing stores.
@@ -359,10 +450,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
             uint32_t v[32];
             tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
             tmem_ld_wait();
+            const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
             uint32_t o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
+                                 __uint_as_float(v[2 * j + 1]) * so);
             const int feat0 = c.f * 256 + acc * 128 + quarter * 32;
             if (feat0 < a.n_out) gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
           }
@@ -371,6 +464,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
         mbar_arrive(tempty_bar);
       }
       acc_phase ^= 1u;
+    }
+    if constexpr (F8 && MODE == kGrpSwiglu) {
+      amax = warp_max(amax);
+      if (lane == 0) atomic_max_nonneg(a.out_amax, amax);
     }
   }
 

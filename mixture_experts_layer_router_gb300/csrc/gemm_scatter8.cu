@@ -1,0 +1,10 @@
+// Latent down-projection with the scatter epilogue writing E4M3 codes of z
+// (the token rows of the E4M3 expert GEMMs) and recording max |z|.
+#include "gemm_launch.cuh"
+
+namespace lmoe {
+cudaError_t launch_gemm_scatter_f8(const GemmMaps& m, const GemmArgs& a, int grid,
+                                   cudaStream_t s) {
+  return launch_gemm_impl<kEpiScatterF8, false>(m, a, grid, s);
+}
+}  // namespace lmoe

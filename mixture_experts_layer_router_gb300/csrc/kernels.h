@@ -22,17 +22,52 @@ cudaError_t launch_gemm_f32(const GemmMaps& m, const GemmArgs& a, int grid, bool
                             cudaStream_t s);
 cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+// kEpiScatterF8: the scatter with E4M3 output (out_scale, out_amax set).
+cudaError_t launch_gemm_scatter_f8(const GemmMaps& m, const GemmArgs& a, int grid,
+                                   cudaStream_t s);
 
-// One launch of gemm_grouped_kernel<mode> (kGrpSwiglu or kGrpPlain):
-// tok = token rows (64-row boxes), w0/w1 = weight rows (128-row boxes).
-cudaError_t launch_gemm_grouped(int mode, const CUtensorMap& tok, const CUtensorMap& w0,
+// One launch of gemm_grouped_kernel<mode, f8> (kGrpSwiglu or kGrpPlain;
+// bf16 or E4M3 operands): tok = token rows (64-row boxes), w0/w1 = packed
+// weight tiles.
+cudaError_t launch_gemm_grouped(int mode, bool f8, const CUtensorMap& tok, const CUtensorMap& w0,
                                 const CUtensorMap& w1, const GroupedArgs& a, int grid,
                                 cudaStream_t s);
 
-// Rewrite W [rows, K] (rows % 128 == 0, K % kGBK == 0) as contiguous
-// 128 x kGBK tiles, tile index (row / 128) * (K / kGBK) + k / kGBK.
-cudaError_t launch_pack_tiles(const __nv_bfloat16* src, __nv_bfloat16* dst, long long rows, int K,
+// Rewrite a row-major matrix of `rows` rows of `row_bytes` bytes (rows % 128
+// == 0, row_bytes % 128 == 0) as contiguous tiles of 128 rows x 128 bytes,
+// tile index (row / 128) * (row_bytes / 128) + byte / 128: kGBK bf16 or
+// kGBK8 E4M3 columns per tile.
+cudaError_t launch_pack_tiles(const void* src, void* dst, long long rows, long long row_bytes,
                               int sms, cudaStream_t s);
+
+// Per-group absolute maximum of bf16 W [groups, rows, cols] (float bits,
+// accumulated with atomicMax into amax_bits[groups], which the caller
+// zeroes), then scale[g] = amax / 448 (1 for an all-zero group).
+cudaError_t launch_absmax_groups(const __nv_bfloat16* src, long long groups, long long group_elems,
+                                 unsigned* amax_bits, int sms, cudaStream_t s);
+cudaError_t launch_scales_from_amax(const unsigned* amax_bits, int n, float* scale,
+                                    cudaStream_t s);
+
+// E4M3 codes of bf16 W [groups * rows_per_group, K] with the group's scale,
+// written either row-major (packed = false) or as the 128 x 128-byte tiles
+// of launch_pack_tiles (packed = true; rows_per_group % 128 == 0, K % 128 == 0).
+cudaError_t launch_quantize_e4m3(const __nv_bfloat16* src, uint8_t* dst, long long rows,
+                                 long long K, long long rows_per_group, const float* scale,
+                                 bool packed, int sms, cudaStream_t s);
+
+// Delayed scaling of n activation tensors (n <= kFp8Tensors): enter this
+// forward's maxima into the 1024-step history, form the next scales, clear
+// the maxima. One launch of one block.
+constexpr int kFp8Tensors = 4;
+constexpr int kFp8History = 1024;
+struct Fp8State {
+  float scale[kFp8Tensors];      // scales the next forward quantizes with
+  unsigned amax[kFp8Tensors];    // maxima being recorded by this forward (float bits)
+  float last_amax[kFp8Tensors];  // maxima of the last finished forward
+  long long steps;               // forwards entered so far
+  float hist[kFp8Tensors][kFp8History];
+};
+cudaError_t launch_fp8_update(Fp8State* st, int n, cudaStream_t s);
 
 // Router GEMM fused with softmax and stable top-k: logits [T,E] fp32 (+bias),
 // idx [T,k], gates [T,k]; x map in 128-row boxes, W_r map in 256-row boxes.

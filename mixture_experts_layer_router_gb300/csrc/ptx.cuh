@@ -188,6 +188,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// Same with kind::f8f6f4 (both operands E4M3 per the instruction
+// descriptor, 32 elements = 32 bytes of K per instruction, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when all tcgen05 ops issued so far by this thread finish.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -253,6 +265,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(const void* tile) {
 // N >> 3 in bits [17,23), M >> 4 in bits [24,29).
 __host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with A and B both E4M3 (format code 0
+// in bits [7,10) and [10,13)), fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t instr_desc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 

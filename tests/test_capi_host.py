@@ -20,7 +20,7 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(latentmoe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(latentmoe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -74,6 +74,16 @@ def test_null_arguments(lib):
     assert lib.latentmoe_load_weights(None, None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_get_status(None, None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_debug_gemm(None, None, None, 1, 128, 128, 0, None) == capi.ERR_INVALID_ARG
+    # E4M3 entries
+    f = (ctypes.c_float * 2)()
+    n = ctypes.c_int64()
+    assert lib.latentmoe_get_fp8_state(None, f, f, ctypes.byref(n)) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_set_fp8_scales(None, f) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_get_fp8_weight_scales(None, f) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_get_fp8_codes(None, None, None, None) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_quantize_e4m3(None, 1, 1, 16, None, None, None) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_debug_grouped_gemm_e4m3(None, None, None, None, None, None, 1, 1, 128,
+                                                 128, 1, None) == capi.ERR_INVALID_ARG
 
 
 def test_strings_and_stages(lib):
@@ -81,5 +91,6 @@ def test_strings_and_stages(lib):
     n = lib.latentmoe_num_stages()
     names = [lib.latentmoe_stage_name(i).decode() for i in range(n)]
     assert names == ["router", "replay_gates", "sort", "down_proj", "expert_gate_up",
-                     "expert_down", "combine", "shared_gate_up", "up_proj"]
+                     "expert_down", "combine", "shared_gate_up", "up_proj",
+                     "fp8_scales"]
     assert lib.latentmoe_stage_name(n) is None

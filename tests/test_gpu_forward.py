@@ -123,7 +123,8 @@ def test_launch_count_and_stage_times():
     assert layer.launch_count() - n0 == 9
     t = layer.stage_times(0)
     assert set(t) == {"router", "replay_gates", "sort", "down_proj", "expert_gate_up",
-                      "expert_down", "combine", "shared_gate_up", "up_proj"}
+                      "expert_down", "combine", "shared_gate_up", "up_proj",
+                      "fp8_scales"}
     assert all(v >= 0 for v in t.values())
 
 
