@@ -5,8 +5,11 @@ latent 3072, 512 experts, top-8, SwiGLU FFN 10240, bf16, ~97 GB of expert
 weights resident). A step is one full forward through the C ABI. Inputs are
 larger than L2 (every step streams all touched expert weights from HBM).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--fp8]
   python bench.py --impl reference ...   # the float64 CPU oracle, rank 0 only
+
+--fp8 runs the expert GEMMs in FP8 E4M3 with delayed scaling (a separate
+metric; the default line is the bf16 forward).
 
 Multi-GPU runs are independent replicas (one process per GPU, weak scaling);
 the only collectives are the timing barrier and the max over ranks.
@@ -28,6 +31,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "LatentMoE bf16 fwd tokens/s at MAI-Base-1 shape; % of tensor-core roofline"
+METRIC_FP8 = ("LatentMoE fwd tokens/s at MAI-Base-1 shape with FP8 E4M3 expert GEMMs; "
+              "% of tensor-core roofline")
+# dense E4M3 tensor rate over dense bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "expert_gate_up"
 GEMM_SRC = os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", "gemm_grouped.cuh")
@@ -40,19 +47,25 @@ def layer_flops_per_token(c) -> int:
     return 2 * c.d * c.E + 2 * c.d * c.l + 6 * c.k * c.l * c.F + 2 * c.l * c.d + 6 * c.d * c.Fs
 
 
-def layer_bytes(c, touched_experts: int) -> int:
-    """Algorithmic bytes: weights read once (experts that got tokens only),
-    x read once, y written once; intermediates excluded as avoidable."""
-    w = touched_experts * 3 * c.l * c.F * 2 + (c.E * c.d + 2 * c.l * c.d + 3 * c.d * c.Fs) * 2
+def expert_flops_per_token(c) -> int:
+    return 6 * c.k * c.l * c.F
+
+
+def layer_bytes(c, touched_experts: int, eb: int = 2) -> int:
+    """Algorithmic bytes: weights read once (experts that got tokens only,
+    eb bytes per expert weight), x read once, y written once; intermediates
+    excluded as avoidable."""
+    w = touched_experts * 3 * c.l * c.F * eb + (c.E * c.d + 2 * c.l * c.d + 3 * c.d * c.Fs) * 2
     return w + c.T * c.d * 2 * 2
 
 
-def gate_up_work(c, touched_experts: int):
+def gate_up_work(c, touched_experts: int, eb: int = 2):
     """Per launch of the grouped gate+up GEMM: FLOPs and algorithmic bytes
-    (gate and up weights of touched experts, z rows read, h rows written)."""
+    (gate and up weights of touched experts, z rows read, h rows written;
+    eb bytes per element: 2 for bf16, 1 for E4M3)."""
     S = c.T * c.k
     flops = 2 * S * c.l * 2 * c.F
-    nbytes = touched_experts * 2 * c.F * c.l * 2 + S * c.l * 2 + S * c.F * 2
+    nbytes = touched_experts * 2 * c.F * c.l * eb + S * c.l * eb + S * c.F * eb
     return flops, nbytes
 
 
@@ -67,10 +80,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, fp8: bool = False):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"{DOMINANT}_{workload}.txt")
+    kernel = DOMINANT + ("_e4m3" if fp8 else "")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         text = open(path).read()
     except OSError:
@@ -151,16 +165,23 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle legs
 
-def oracle_tokens_per_s(cfg, x_rows, logits_rows, fetch, repeats=1):
-    """Time the float64 oracle on given token rows; returns (tokens/s, s)."""
+def oracle_tokens_per_s(cfg, x_rows, logits_rows, fetch, repeats=1, fp8_scales=None):
+    """Time the float64 oracle on given token rows; returns (tokens/s, s).
+    With fp8_scales (s_z, s_h) the oracle's E4M3 expert layer is timed."""
     from oracle import latentmoe_ref as ref
+    from oracle import fp8 as ofp8
     import numpy as np
     W = ref.OracleWeights(fetch["w_r"], fetch["w_dn"], fetch["w_up"], fetch["expert"],
                           b_r=fetch["b_r"], w_gs=fetch["w_gs"], w_us=fetch["w_us"],
                           w_ds=fetch["w_ds"])
     t0 = time.perf_counter()
     for _ in range(repeats):
-        ref.forward(np.asarray(x_rows, dtype=np.float64), W, cfg.k, logits=logits_rows)
+        xr = np.asarray(x_rows, dtype=np.float64)
+        if fp8_scales is None:
+            ref.forward(xr, W, cfg.k, logits=logits_rows)
+        else:
+            ofp8.forward_fp8(xr, W, cfg.k, s_z=fp8_scales[0], s_h=fp8_scales[1],
+                             logits=logits_rows)
     dt = time.perf_counter() - t0
     return x_rows.shape[0] * repeats / dt, dt
 
@@ -270,8 +291,9 @@ def run_ours(args, cfg, rank, world, dist):
     capi.load()
     w = synth.make_weights(cfg, 0, "cuda")
     x = synth.make_x(cfg, 0, "cuda")
+    f8 = args.fp8
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
-                           router_bias=w["b_r"] is not None)
+                           router_bias=w["b_r"] is not None, fp8=f8)
     layer.load_weights(w)
     # the library holds its own (packed) copy; the expert weights the CPU
     # baseline needs are regenerated from their per-expert seeds
@@ -284,6 +306,7 @@ def run_ours(args, cfg, rank, world, dist):
         layer.forward(x, y)
     torch.cuda.synchronize()
     assert layer.status() == 0, "device status set during warm-up"
+    fp8_state = layer.fp8_state() if f8 else None
     r = layer.get_routing(cfg.T, "cuda")
     counts = r["counts"].cpu().numpy()
     touched = int((counts > 0).sum())
@@ -347,39 +370,51 @@ def run_ours(args, cfg, rank, world, dist):
         need = sorted(set(r["idx"][tsel].cpu().numpy().ravel().tolist()))
         fetch = host_weights(cfg, w, need)
         xs = x[tsel].float().cpu().numpy().astype(np.float64)
-        tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch)
+        scales = layer.fp8_state()["scales"] if f8 else None
+        tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch, fp8_scales=scales)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
                "sample": f"{n} seeded tokens of the {cfg.name} workload ({dt:.1f} s), float64 "
-                         "NumPy oracle routed from the GPU logits, expert weights upcast from "
-                         "host bf16 inside the timed work"}
+                         "NumPy oracle" + (" (E4M3 experts at the GPU's scales)" if f8 else "") +
+                         " routed from the GPU logits, expert weights upcast from host bf16 "
+                         "inside the timed work"}
 
     peaks, peak_src = load_peaks()
     ms_step = ms_total / args.steps
     value = world * cfg.T * args.steps / (ms_total / 1e3)
     flops_tok = layer_flops_per_token(cfg)
-    lbytes = layer_bytes(cfg, touched)
-    tc_ms = cfg.T * flops_tok / (peaks["bf16_tflops_sustained"] * 1e12) * 1e3
+    eb = 1 if f8 else 2
+    lbytes = layer_bytes(cfg, touched, eb)
+    bf16_peak = peaks["bf16_tflops_sustained"] * 1e12
+    # expert FLOPs at the E4M3 rate when they run in E4M3
+    x_flops = cfg.T * expert_flops_per_token(cfg)
+    o_flops = cfg.T * flops_tok - x_flops
+    tc_ms = (o_flops / bf16_peak + x_flops / (bf16_peak * (FP8_OVER_BF16 if f8 else 1.0))) * 1e3
     hbm_ms = lbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
-    g_flops, g_bytes = gate_up_work(cfg, touched)
+    g_flops, g_bytes = gate_up_work(cfg, touched, eb)
     g_ms = stage_ms.get(DOMINANT, float("nan"))
-    g_tc = g_flops / (peaks["bf16_tflops_sustained"] * 1e12) * 1e3
+    g_peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if f8 else 1.0)
+    g_tc = g_flops / (g_peak * 1e12) * 1e3
     g_hbm = g_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
     if g_hbm >= g_tc:
         roof = {"bound": "hbm", "achieved": g_bytes / (g_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
         roof = {"bound": "tensor", "achieved": g_flops / (g_ms / 1e3) / 1e12,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+                "peak": g_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic(cfg.name)
-    roof.update({"kernel": DOMINANT, "ms_per_launch": g_ms, "algorithmic_bytes": g_bytes,
-                 "flops": g_flops, "tensor_tflops": g_flops / (g_ms / 1e3) / 1e12,
-                 "peak_source": f"{peak_src} ({'sustained bf16' if roof['bound'] == 'tensor' else 'HBM copy'})"})
+    roof["traffic"] = profiled_traffic(cfg.name, f8)
+    peak_kind = ("sustained bf16 x 2 for E4M3" if f8 else "sustained bf16") \
+        if roof["bound"] == "tensor" else "HBM copy"
+    roof.update({"kernel": DOMINANT + ("_e4m3" if f8 else ""), "ms_per_launch": g_ms,
+                 "algorithmic_bytes": g_bytes, "flops": g_flops,
+                 "tensor_tflops": g_flops / (g_ms / 1e3) / 1e12,
+                 "peak_source": f"{peak_src} ({peak_kind})"})
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC_FP8 if f8 else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 experts, bf16 elsewhere" if f8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
         "config": workload_config(cfg),
         "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
@@ -396,6 +431,9 @@ def run_ours(args, cfg, rank, world, dist):
         "clocks": clk,
         "device_status": status,
     }
+    if f8:
+        line["fp8_scales"] = {"z": fp8_state["scales"][0], "h": fp8_state["scales"][1],
+                              "history_steps": fp8_state["steps"]}
     return line
 
 
@@ -406,13 +444,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mai-base-1")
-    ap.add_argument("--cpu-tokens", type=int, default=48)
+    ap.add_argument("--cpu-tokens", type=int, default=None,
+                    help="oracle sample for cpu_baseline (default 48 tokens; 2 with --fp8, "
+                         "whose oracle quantizes each touched expert's weights)")
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 E4M3 expert GEMMs with delayed scaling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.cpu_tokens is None:
+        args.cpu_tokens = 2 if args.fp8 else 48
 
     from mixture_experts_layer_router_gb300 import synth
     cfg = synth.CONFIGS[args.config]

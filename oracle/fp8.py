@@ -135,9 +135,7 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
     zq_slots = quantize_act(z, s_z)[perm] if z_codes is None else \
         np.asarray(z_codes, dtype=np.float64)
     H = np.zeros((perm.shape[0], z.shape[1]), dtype=np.float64)
-    F = weights.expert(0)[0].shape[0]
-    h_all = np.zeros((perm.shape[0], F), dtype=np.float64)
-    hq_all = np.zeros((perm.shape[0], F), dtype=np.float64)
+    h_all = hq_all = None  # [T*k, F], allocated once F is known
     h_amax = 0.0
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
@@ -154,6 +152,9 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         h_amax = max(h_amax, float(np.abs(h).max()))
         qh = quantize_act(h, s_h) if h_codes is None else \
             np.asarray(h_codes[lo:hi], dtype=np.float64)
+        if h_all is None:
+            h_all = np.zeros((perm.shape[0], w_g.shape[0]), dtype=np.float64)
+            hq_all = np.zeros_like(h_all)
         h_all[lo:hi] = h
         hq_all[lo:hi] = qh
         H[lo:hi] = (qh @ qd.T) * (s_h * sd)
