@@ -116,13 +116,16 @@ def quantize_act(t: np.ndarray, s: float) -> np.ndarray:
 def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s_h: float,
                 renorm: bool = False, logits: Optional[np.ndarray] = None,
                 z_codes: Optional[np.ndarray] = None,
-                h_codes: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+                h_codes: Optional[np.ndarray] = None,
+                wq_cache: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """The layer with FP8 E4M3 expert GEMMs; everything else as ref.forward.
 
     z_codes [T*k, l] / h_codes [T*k, F] (E4M3 code values, slot order), when
     given, replace the codes this function would form for z and h: the
     expert GEMMs are then evaluated on exactly those codes. The returned
-    "z_q" and "h_q" are the codes used, and "h" the unquantized h."""
+    "z_q" and "h_q" are the codes used, and "h" the unquantized h.
+    wq_cache, a dict kept by the caller, holds each expert's quantized
+    weights across calls on the same weights."""
     x = np.asarray(x, dtype=np.float64)
     E = weights.num_experts
     L = ref.router_logits(x, weights.w_r, weights.b_r) if logits is None else \
@@ -141,10 +144,15 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue
-        w_g, w_u, w_d = weights.expert(e)
-        qg, sg = quantize_weight(w_g)
-        qu, su = quantize_weight(w_u)
-        qd, sd = quantize_weight(w_d)
+        if wq_cache is not None and e in wq_cache:
+            (qg, sg), (qu, su), (qd, sd) = wq_cache[e]
+        else:
+            w_g, w_u, w_d = weights.expert(e)
+            qg, sg = quantize_weight(w_g)
+            qu, su = quantize_weight(w_u)
+            qd, sd = quantize_weight(w_d)
+            if wq_cache is not None:
+                wq_cache[e] = ((qg, sg), (qu, su), (qd, sd))
         zq = zq_slots[lo:hi]
         gate = (zq @ qg.T) * (s_z * sg)
         up = (zq @ qu.T) * (s_z * su)
@@ -153,7 +161,7 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         qh = quantize_act(h, s_h) if h_codes is None else \
             np.asarray(h_codes[lo:hi], dtype=np.float64)
         if h_all is None:
-            h_all = np.zeros((perm.shape[0], w_g.shape[0]), dtype=np.float64)
+            h_all = np.zeros((perm.shape[0], qg.shape[0]), dtype=np.float64)
             hq_all = np.zeros_like(h_all)
         h_all[lo:hi] = h
         hq_all[lo:hi] = qh

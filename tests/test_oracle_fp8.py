@@ -227,3 +227,13 @@ def test_given_codes_reproduce_own_codes():
     # slot i holds token perm[i]'s latent codes
     z = ref.latent_down(w["x"], W.w_dn)
     assert np.array_equal(a["z_q"], fp8.quantize_act(z, 0.01)[a["perm"]])
+
+
+def test_weight_cache_changes_nothing():
+    w = oracle_pins.tiny_layer(84, T=20, d=16, l=32, E=4, k=2, F=32)
+    W = oracle_pins.oracle_weights(ref, w)
+    cache = {}
+    a = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003)
+    b = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, wq_cache=cache)
+    c = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, wq_cache=cache)
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["y"], c["y"]) and cache
