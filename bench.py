@@ -37,7 +37,8 @@ METRIC_FP8 = ("LatentMoE fwd tokens/s at MAI-Base-1 shape with FP8 E4M3 expert G
 FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "expert_gate_up"
-GEMM_SRC = os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", "gemm_grouped.cuh")
+GEMM_SRC = [os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", f)
+            for f in ("gemm_grouped.cuh", "gemm_grouped2.cuh")]
 
 
 # ---------------------------------------------------------------- arithmetic
@@ -93,7 +94,10 @@ def profiled_traffic(workload: str, fp8: bool = False):
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not (m_sha and m_tr):
         return None
-    cur = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for f in GEMM_SRC:
+        h.update(open(f, "rb").read())
+    cur = h.hexdigest()
     return float(m_tr.group(1)) if m_sha.group(1) == cur else None
 
 
@@ -295,6 +299,8 @@ def run_ours(args, cfg, rank, world, dist):
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
                            router_bias=w["b_r"] is not None, fp8=f8)
     layer.load_weights(w)
+    if args.no_sm_pairs:
+        layer.set_sm_pairs(False)
     # the library holds its own (packed) copy; the expert weights the CPU
     # baseline needs are regenerated from their per-expert seeds
     for key in ("w_g", "w_u", "w_d"):
@@ -416,7 +422,8 @@ def run_ours(args, cfg, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 experts, bf16 elsewhere" if f8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
-        "config": workload_config(cfg),
+        "config": {**workload_config(cfg),
+                   "expert_gemm": "single-SM" if args.no_sm_pairs else "SM pairs where shapes allow"},
         "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
         "tc_roofline_frac": tc_ms / ms_step,
         "layer_roofline": {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms,
@@ -452,6 +459,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 E4M3 expert GEMMs with delayed scaling")
+    ap.add_argument("--no-sm-pairs", action="store_true",
+                    help="expert GEMMs on single SMs instead of SM pairs (comparison runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -291,6 +291,13 @@ int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count);
 int latentmoe_num_stages(void);
 const char* latentmoe_stage_name(int stage);
 
+/* Expert GEMMs on SM pairs (enable = 1, the default) or on single SMs (0).
+ * The pair kernels run tcgen05 MMAs with M = 256 over two SMs of a cluster,
+ * each SM holding half of the token tile; they are used where the shapes
+ * allow (gate+up: F % 256 == 0; down: l % 512 == 0) and the single-SM
+ * kernels elsewhere. Takes effect at the next forward. */
+int latentmoe_set_sm_pairs(latentmoe_t h, int enable);
+
 /* Kernel launches issued by this handle since creation. */
 int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches);
 
@@ -310,7 +317,9 @@ const char* latentmoe_strerror(int code);
  * M >= 1, K and N multiples of 128 (mode 1: N >= 1). Grouped variant: rows
  * of A and C are split by device int32 offsets [G+1] (offsets[0] = 0,
  * non-decreasing, offsets[G] <= M, G <= 512); group g multiplies with rows
- * [g*N, (g+1)*N) of B (of each half of B in mode 2).
+ * [g*N, (g+1)*N) of B (of each half of B in mode 2). In the grouped
+ * variant, mode | 4 runs the SM-pair kernel (modes 0 and 2; N % 512 == 0
+ * in mode 0, N % 256 == 0 in mode 2).
  * Asynchronous on `stream`; errors as above. */
 int latentmoe_debug_gemm(const void* A, const void* B, void* C, int64_t M,
                          int64_t N, int64_t K, int mode,
@@ -328,7 +337,8 @@ int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C,
  *           / s_out); amax (device, one uint32, caller-zeroed) receives the
  *           float bits of max |h| over all rows
  * Groups as in latentmoe_debug_grouped_gemm. K and N multiples of 128.
- * Synchronises `stream`. */
+ * mode | 4 runs the SM-pair kernel (N % 512 == 0 in mode 1, N % 256 == 0 in
+ * mode 2). Synchronises `stream`. */
 int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B,
                                       const float* scales, void* C, uint32_t* amax,
                                       const int32_t* offsets, int64_t groups,

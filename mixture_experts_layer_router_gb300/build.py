@@ -22,7 +22,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liblatentmoe.so")
 
 SOURCES = ["api.cu", "route.cu", "combine.cu", "gemm_bf16.cu", "gemm_f32.cu",
-           "gemm_swiglu.cu", "gemm_scatter.cu", "gemm_scatter8.cu", "gemm_grouped.cu", "pack.cu",
+           "gemm_swiglu.cu", "gemm_scatter.cu", "gemm_scatter8.cu", "gemm_grouped.cu", "gemm_grouped2.cu",
+           "pack.cu",
            "router.cu", "route_static.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

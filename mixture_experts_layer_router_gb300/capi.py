@@ -69,6 +69,7 @@ SIGNATURES = {
     "latentmoe_num_stages": (ctypes.c_int, []),
     "latentmoe_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
     "latentmoe_get_launch_count": (ctypes.c_int, [_c_void_p, ctypes.POINTER(_i64)]),
+    "latentmoe_set_sm_pairs": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
     "latentmoe_last_cuda_error": (ctypes.c_int, [_c_void_p]),
     "latentmoe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "latentmoe_debug_gemm": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
@@ -113,15 +114,18 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 class LatentMoEError(RuntimeError):
-    def __init__(self, code: int, what: str):
+    def __init__(self, code: int, what: str, cuda_error: int = 0):
         self.code = code
+        self.cuda_error = cuda_error
         msg = load().latentmoe_strerror(code).decode()
-        super().__init__(f"{what}: {msg} ({code})")
+        extra = f", cudaError {cuda_error}" if cuda_error else ""
+        super().__init__(f"{what}: {msg} ({code}{extra})")
 
 
-def check(code: int, what: str) -> None:
+def check(code: int, what: str, handle=None) -> None:
     if code != OK:
-        raise LatentMoEError(code, what)
+        cuda = load().latentmoe_last_cuda_error(handle) if handle is not None else 0
+        raise LatentMoEError(code, what, cuda)
 
 
 def _ptr(t) -> Optional[int]:
@@ -169,7 +173,7 @@ class LatentMoE:
                                  ("w_r", "b_r", "w_dn", "w_g", "w_u", "w_d", "w_up",
                                   "w_gs", "w_us", "w_ds")))
         check(load().latentmoe_load_weights(self.handle, ctypes.byref(lw)),
-              "latentmoe_load_weights")
+              "latentmoe_load_weights", self.handle)
 
     def forward(self, x, out=None, stream=None):
         import torch
@@ -178,7 +182,7 @@ class LatentMoE:
             dt = torch.float32 if self.flags & OUT_FP32 else torch.bfloat16
             out = torch.empty((T, self.dims.hidden), dtype=dt, device=x.device)
         check(load().latentmoe_forward(self.handle, x.data_ptr(), out.data_ptr(), T,
-                                       _stream(stream)), "latentmoe_forward")
+                                       _stream(stream)), "latentmoe_forward", self.handle)
         return out
 
     def forward_routed(self, x, idx, gates=None, out=None, stream=None):
@@ -190,7 +194,7 @@ class LatentMoE:
             out = torch.empty((T, self.dims.hidden), dtype=dt, device=x.device)
         check(load().latentmoe_forward_routed(self.handle, x.data_ptr(), idx.data_ptr(),
                                               _ptr(gates), out.data_ptr(), T, _stream(stream)),
-              "latentmoe_forward_routed")
+              "latentmoe_forward_routed", self.handle)
         return out
 
     def forward_host(self, x_host, out_host, stream=None):
@@ -292,6 +296,10 @@ class LatentMoE:
         check(load().latentmoe_get_fp8_weight_scales(self.handle, buf),
               "latentmoe_get_fp8_weight_scales")
         return [list(buf[m * E:(m + 1) * E]) for m in range(3)]
+
+    def set_sm_pairs(self, enable: bool) -> None:
+        check(load().latentmoe_set_sm_pairs(self.handle, int(enable)),
+              "latentmoe_set_sm_pairs")
 
     def launch_count(self) -> int:
         v = _i64(0)

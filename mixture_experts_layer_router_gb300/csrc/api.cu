@@ -145,6 +145,7 @@ struct latentmoe {
   int sms = 1;
   bool loaded = false;
   bool fp8 = false;             // E4M3 expert GEMMs
+  bool sm_pairs = true;         // SM-pair grouped kernels where the shapes allow
   latentmoe_weights w;          // the library-owned copies below
   float* w_scale = nullptr;     // E4M3: [3E] scales of W_g, W_u, W_d per expert (in wmem)
   lmoe::Fp8State* f8 = nullptr; // E4M3: delayed-scaling state (in ws)
@@ -617,8 +618,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       a.out_scale = &h->f8->scale[1];
       a.out_amax = &h->f8->amax[1];
     }
-    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu, a,
-                                         h->sms, s));
+    if (h->sm_pairs && F % 256 == 0) {
+      a.fblocks = F / 256;
+      LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu,
+                                                a, h->sms, s));
+    } else {
+      LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu, a,
+                                           h->sms, s));
+    }
     h->launches += 1;
   }
   record(h, slot_base, 5, s);
@@ -639,8 +646,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       a.w_scale0 = a.w_scale1 = h->w_scale + 2 * E;
       a.in_scale = &h->f8->scale[1];
     }
-    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd, a,
-                                         h->sms, s));
+    if (h->sm_pairs && l % 512 == 0) {
+      a.fblocks = l / 512;
+      LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd,
+                                                a, h->sms, s));
+    } else {
+      LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd, a,
+                                           h->sms, s));
+    }
     h->launches += 1;
   }
   record(h, slot_base, 6, s);
@@ -848,6 +861,12 @@ int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count) {
   return LATENTMOE_OK;
 }
 
+int latentmoe_set_sm_pairs(latentmoe_t h, int enable) {
+  if (h == nullptr || (enable != 0 && enable != 1)) return LATENTMOE_ERR_INVALID_ARG;
+  h->sm_pairs = enable != 0;
+  return LATENTMOE_OK;
+}
+
 int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches) {
   if (h == nullptr || launches == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   *launches = h->launches;
@@ -949,9 +968,13 @@ unsigned* debug_status_word() {
 }
 
 int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offsets, int64_t G,
-                    int64_t M, int64_t N, int64_t K, int mode, cudaStream_t s) {
-  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || mode < 0 || mode > 2)
+                    int64_t M, int64_t N, int64_t K, int mode_bits, cudaStream_t s) {
+  const bool pair = (mode_bits & 4) != 0;
+  const int mode = mode_bits & ~4;
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || mode < 0 || mode > 2 ||
+      (pair && (offsets == nullptr || mode == 1)))
     return LATENTMOE_ERR_INVALID_ARG;
+  if (pair && ((mode == 2 && N % 256) || (mode == 0 && N % 512))) return LATENTMOE_ERR_UNSUPPORTED;
   if (K % 128 || (mode != 1 && N % 128) || M > (1 << 30) || N > (1 << 20))
     return LATENTMOE_ERR_UNSUPPORTED;
   if (offsets && (G < 1 || G > lmoe::kMaxGroups)) return LATENTMOE_ERR_UNSUPPORTED;
@@ -994,8 +1017,15 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
     ga.out = C;
     ga.ldo = N;
     ga.status = status;
-    cudaError_t e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain,
-                                              false, tok, w0, w1, ga, num_sms(), s);
+    cudaError_t e;
+    if (pair) {
+      ga.fblocks = static_cast<int>(mode == 2 ? N / 256 : N / 512);
+      e = lmoe::launch_gemm_grouped_pair(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false,
+                                         tok, w0, w1, ga, num_sms(), s);
+    } else {
+      e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false, tok,
+                                    w0, w1, ga, num_sms(), s);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(bp);
     return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
@@ -1052,11 +1082,14 @@ int latentmoe_debug_grouped_gemm(const void* A, const void* B, void* C, const in
 
 int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B, const float* scales,
                                       void* C, uint32_t* amax, const int32_t* offsets,
-                                      int64_t G, int64_t M, int64_t N, int64_t K, int mode,
+                                      int64_t G, int64_t M, int64_t N, int64_t K, int mode_bits,
                                       latentmoe_stream_t st) {
+  const bool pair = (mode_bits & 4) != 0;
+  const int mode = mode_bits & ~4;
   if (!A || !B || !scales || !C || !offsets || M < 1 || N < 1 || K < 1 || G < 1 ||
       (mode != 1 && mode != 2) || (mode == 2 && amax == nullptr))
     return LATENTMOE_ERR_INVALID_ARG;
+  if (pair && ((mode == 2 && N % 256) || (mode == 1 && N % 512))) return LATENTMOE_ERR_UNSUPPORTED;
   if (K % 128 || N % 128 || M > (1 << 30) || N > (1 << 20) || G > lmoe::kMaxGroups)
     return LATENTMOE_ERR_UNSUPPORTED;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) ||
@@ -1103,8 +1136,15 @@ int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B, const 
   ga.w_scale0 = scales + 2;
   ga.w_scale1 = mode == 2 ? scales + 2 + G : scales + 2;
   ga.out_amax = amax;
-  cudaError_t e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, true,
-                                            tok, w0, w1, ga, num_sms(), s);
+  cudaError_t e;
+  if (pair) {
+    ga.fblocks = static_cast<int>(mode == 2 ? N / 256 : N / 512);
+    e = lmoe::launch_gemm_grouped_pair(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, true, tok,
+                                       w0, w1, ga, num_sms(), s);
+  } else {
+    e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, true, tok, w0,
+                                  w1, ga, num_sms(), s);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   cudaFree(bp);
   return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;

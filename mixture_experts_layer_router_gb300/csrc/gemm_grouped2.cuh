@@ -1,0 +1,383 @@
+// Grouped expert GEMM on SM pairs: the grouped kernel of gemm_grouped.cuh
+// with tcgen05 MMAs of cta_group::2 (M = 256 over two SMs).
+//
+// A pair tile is 256 weight rows per accumulator x the expert's tokens of one
+// chunk (N <= 256, a multiple of 16). Each CTA of the pair holds its 128
+// weight rows of both accumulators and half of the token rows (N/2), and
+// receives its 128 rows of both accumulators in its own TMEM. Per k-block a
+// CTA therefore takes in 32 KB of weights + 16 KB of tokens (against 32 + 32
+// on one SM) and its tensor core reads 64 KB of shared memory (against 96),
+// for the same MACs per SM: the operand feed that bounds the one-SM kernel
+// shrinks by about 1.4x.
+//
+//   SwiGLU: CTA r holds feature block 2p + r (gate rows in accumulator 0, up
+//           rows in accumulator 1) of pair tile p; its epilogue is the one-SM
+//           SwiGLU epilogue for those 128 features.
+//   plain:  accumulator a covers rows 512p + 256a .. +256 of W_d; CTA r holds
+//           rows 512p + 256a + 128r .. +128.
+//
+// Roles (both CTAs): warp 0 lane 0 loads its CTA's tiles (completing on the
+// leader's full barrier), warp 1 allocates TMEM (the leader's lane 0 also
+// issues the MMAs and commits to both CTAs), warps 2..9 drain this CTA's
+// accumulators and arrive, one lane per warp, on the leader's TMEM-empty
+// barrier. Pair rules are listed in ptx_pair.cuh.
+//
+// Shapes: SwiGLU needs F % 256 == 0, plain needs l % 512 == 0 (otherwise the
+// one-SM kernel runs).
+#pragma once
+
+#include "gemm_grouped.cuh"
+#include "ptx_pair.cuh"
+
+namespace lmoe {
+
+constexpr int kPStages = 4;
+constexpr int kPTokenTile = 128 * 128;  // up to 128 token rows of 128 bytes
+constexpr int kPStageBytes = 2 * kGWeightTile + kPTokenTile;  // 48 KB
+constexpr int kPBarrierBytes = 8 * (2 * kPStages + 3);
+constexpr int kPSmemBytes = 1024 + kPStages * kPStageBytes + kPBarrierBytes + 16 +
+                            2 * (kGMaxGroups + 1) * 4 + kGEpiWarps * kGStageWarpBytes;
+static_assert(kPSmemBytes <= 232448, "pair kernel shared memory");
+
+struct PTile {
+  int g;      // group
+  int tok0;   // first token row of the chunk
+  int len;    // valid tokens (<= 256)
+  int n;      // MMA N: len rounded up to 16
+  int p;      // pair feature block
+};
+
+__device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const int* seg_s,
+                                              const int* tp_s) {
+  int lo = 0, hi = a.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tp_s[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int n = seg_s[g + 1] - seg_s[g];
+  int nch, cs;
+  group_chunks(n, nch, cs);
+  const int local = t - tp_s[g];
+  const int p = local / nch;
+  const int c = local - p * nch;
+  PTile r;
+  r.g = g;
+  r.tok0 = seg_s[g] + c * cs;
+  r.len = min(cs, n - c * cs);
+  r.n = (r.len + 15) & ~15;
+  r.p = p;
+  return r;
+}
+
+// a.fblocks = pair feature blocks per group (SwiGLU F/256, plain l/512).
+template <int MODE, bool F8>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmTok,
+                             const __grid_constant__ CUtensorMap tmW0,
+                             const __grid_constant__ CUtensorMap tmW1, const GroupedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kPStages * kPStageBytes);
+  uint64_t* empty_bar = full_bar + kPStages;
+  uint64_t* tfull_bar = empty_bar + kPStages;
+  uint64_t* tempty_bar = tfull_bar + 1;
+  uint64_t* done_bar = tempty_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
+  int* tp_s = seg_s + kGMaxGroups + 1;
+  uint8_t* stage_smem = reinterpret_cast<uint8_t*>(tp_s + kGMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const uint32_t peer_abort =
+      mapa_shared(smem_addr(const_cast<int*>(abort_flag)), rank ^ 1u);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * kGEpiWarps);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmTok);
+    tma_prefetch_desc(&tmW0);
+    tma_prefetch_desc(&tmW1);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
+  __syncthreads();
+  if (warp == 2) {
+    // exclusive prefix over groups of (token chunks x pair feature blocks)
+    int carry = 0;
+    if (lane == 0) tp_s[0] = 0;
+    for (int base = 0; base < a.num_groups; base += 32) {
+      const int g = base + lane;
+      int v = 0;
+      if (g < a.num_groups) {
+        const int n = seg_s[g + 1] - seg_s[g];
+        if (n > 0) {
+          int nch, cs;
+          group_chunks(n, nch, cs);
+          v = nch * a.fblocks;
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (g < a.num_groups) tp_s[g + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_sync();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tp_s[a.num_groups];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      const uint64_t pol_w = policy_evict_normal();
+      const uint64_t pol_t = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = pair; t < total_tiles && ok; t += npairs) {
+        const PTile c = decode_ptile(t, a, seg_s, tp_s);
+        const int half = c.n >> 1;
+        const int nbox = (half + kGTokBox - 1) / kGTokBox;
+        const uint32_t bytes = 2u * (2 * kGWeightTile + nbox * kGTokBoxBytes);
+        int rt0, rt1;
+        if (MODE == kGrpSwiglu) {
+          rt0 = rt1 = (c.g * a.w_group_rows) / 128 + 2 * c.p + static_cast<int>(rank);
+        } else {
+          rt0 = (c.g * a.w_group_rows) / 128 + 4 * c.p + static_cast<int>(rank);
+          rt1 = rt0 + 2;
+        }
+        const int tok_row = c.tok0 + static_cast<int>(rank) * half;
+        for (int kb = 0; kb < a.kb; ++kb) {
+          if (!wait_bounded_pair(&empty_bar[stage], phase ^ 1u, abort_flag, peer_abort,
+                                 a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw0 = tiles + stage * kPStageBytes;
+          uint8_t* sw1 = sw0 + kGWeightTile;
+          uint8_t* stok = sw1 + kGWeightTile;
+          const uint32_t fb = mapa_shared(smem_addr(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          tma_load_3d_pair(&tmW0, fb, sw0, 0, 0, rt0 * a.kb + kb, pol_w);
+          tma_load_3d_pair(MODE == kGrpSwiglu ? &tmW1 : &tmW0, fb, sw1, 0, 0, rt1 * a.kb + kb,
+                           pol_w);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d_pair(&tmTok, fb, stok + b * kGTokBoxBytes, kb * (F8 ? kGBK8 : kGBK),
+                             tok_row + b * kGTokBox, pol_t);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the leader's full barriers count both CTAs' bytes: waiting on them
+      // drains every copy of the pair still in flight
+      if (leader)
+        for (int s = 0; s < kPStages; ++s)
+          if (issued_mask & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (leader)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = pair; t < total_tiles && ok; t += npairs) {
+        const PTile c = decode_ptile(t, a, seg_s, tp_s);
+        const uint32_t idesc = F8 ? instr_desc_e4m3(256, c.n) : instr_desc_bf16(256, c.n);
+        if (!wait_bounded_pair(tempty_bar, acc_phase ^ 1u, abort_flag, peer_abort, a.status))
+          break;
+        tc_fence_after_sync();
+        for (int kb = 0; kb < a.kb; ++kb) {
+          if (!wait_bounded_pair(&full_bar[stage], phase, abort_flag, peer_abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint8_t* sw0 = tiles + stage * kPStageBytes;
+          const uint64_t d0 = smem_desc_sw128(sw0);
+          const uint64_t d1 = smem_desc_sw128(sw0 + kGWeightTile);
+          const uint64_t dt = smem_desc_sw128(sw0 + 2 * kGWeightTile);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            if constexpr (F8) {
+              tc_mma_pair_f8(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+              tc_mma_pair_f8(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            } else {
+              tc_mma_pair(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+              tc_mma_pair(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            }
+          }
+          tc_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == kPStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(tfull_bar, 0x3);
+        acc_phase ^= 1u;
+      }
+      tc_commit_pair(done_bar, 0x3);
+      wait_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps (both CTAs)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* stage_w = stage_smem + (warp - 2) * kGStageWarpBytes;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tempty_leader = mapa_shared(smem_addr(tempty_bar), 0);
+    uint32_t acc_phase = 0;
+    const float in_s = F8 ? *a.in_scale : 1.0f;
+    const float out_inv = (F8 && MODE == kGrpSwiglu) ? inv_scale(*a.out_scale) : 1.0f;
+    float amax = 0.0f;
+    for (int t = pair; t < total_tiles; t += npairs) {
+      const PTile c = decode_ptile(t, a, seg_s, tp_s);
+      if (!warp_wait_bounded_pair(tfull_bar, acc_phase, abort_flag, peer_abort, a.status)) break;
+      tc_fence_after_sync();
+      const int nchunks = (c.len + 31) / 32;
+      if constexpr (MODE == kGrpSwiglu) {
+        const int fblock = 2 * c.p + static_cast<int>(rank);
+        const int feat0 = fblock * 128 + quarter * 32;
+        if constexpr (F8) {
+          const float sg = in_s * a.w_scale0[c.g], su = in_s * a.w_scale1[c.g];
+          uint32_t hq[4][8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = half + 2 * i;
+            if (ch < nchunks) {
+              uint32_t g[32], u[32];
+              tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
+              tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
+              tmem_ld_wait();
+              const int valid = c.len - ch * 32;
+              float hv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                hv[j] = silu(__uint_as_float(g[j]) * sg) * (__uint_as_float(u[j]) * su);
+                if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                hq[i][j] = quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3],
+                                       out_inv);
+            }
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = half + 2 * i;
+            if (ch < nchunks)
+              gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+                              c.len - ch * 32, feat0);
+          }
+        } else {
+          uint32_t hp[4][16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = half + 2 * i;
+            if (ch < nchunks) {
+              uint32_t g[32], u[32];
+              tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
+              tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                hp[i][j] = pack_bf16x2(
+                    silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]),
+                    silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+            }
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = half + 2 * i;
+            if (ch < nchunks)
+              gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+                           c.len - ch * 32, feat0);
+          }
+        }
+      } else {
+        const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
+        for (int ch = half; ch < nchunks; ch += 2) {
+          const long long tok_row0 = static_cast<long long>(c.tok0) + ch * 32;
+          const int tok_valid = c.len - ch * 32;
+#pragma unroll 1
+          for (int acc = 0; acc < 2; ++acc) {
+            uint32_t v[32];
+            tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
+            tmem_ld_wait();
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
+                                 __uint_as_float(v[2 * j + 1]) * so);
+            const int feat0 = c.p * 512 + acc * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+            gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader);
+      }
+      acc_phase ^= 1u;
+    }
+    if constexpr (F8 && MODE == kGrpSwiglu) {
+      amax = warp_max(amax);
+      if (lane == 0) atomic_max_nonneg(a.out_amax, amax);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  // every MMA of the pair has completed (the leader waited on its last
+  // commit) and both epilogues are done with TMEM
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+}  // namespace lmoe

@@ -33,6 +33,14 @@ cudaError_t launch_gemm_grouped(int mode, bool f8, const CUtensorMap& tok, const
                                 const CUtensorMap& w1, const GroupedArgs& a, int grid,
                                 cudaStream_t s);
 
+// The same GEMMs on SM pairs (clusters of 2, tcgen05 cta_group::2):
+// a.fblocks counts pair feature blocks (SwiGLU: F / 256; plain: l / 512).
+// Needs F % 256 == 0 (SwiGLU) or l % 512 == 0 (plain). Grid: as many pairs
+// as can be resident at once, at most sms / 2.
+cudaError_t launch_gemm_grouped_pair(int mode, bool f8, const CUtensorMap& tok,
+                                     const CUtensorMap& w0, const CUtensorMap& w1,
+                                     const GroupedArgs& a, int sms, cudaStream_t s);
+
 // Rewrite a row-major matrix of `rows` rows of `row_bytes` bytes (rows % 128
 // == 0, row_bytes % 128 == 0) as contiguous tiles of 128 rows x 128 bytes,
 // tile index (row / 128) * (row_bytes / 128) + byte / 128: kGBK bf16 or
