@@ -301,6 +301,8 @@ def run_ours(args, cfg, rank, world, dist):
     layer.load_weights(w)
     if args.no_sm_pairs:
         layer.set_sm_pairs(False)
+    if args.capacity > 0:
+        layer.set_capacity(args.capacity, args.group_size, args.max_rounds)
     # the library holds its own (packed) copy; the expert weights the CPU
     # baseline needs are regenerated from their per-expert seeds
     for key in ("w_g", "w_u", "w_d"):
@@ -313,6 +315,11 @@ def run_ours(args, cfg, rank, world, dist):
     torch.cuda.synchronize()
     assert layer.status() == 0, "device status set during warm-up"
     fp8_state = layer.fp8_state() if f8 else None
+    rounds_info = None
+    if args.capacity > 0:
+        ri = layer.rounds()
+        rounds_info = {"needed": ri["needed"], "launched": ri["launched"],
+                       "left_over": ri["left_over"]}
     r = layer.get_routing(cfg.T, "cuda")
     counts = r["counts"].cpu().numpy()
     touched = int((counts > 0).sum())
@@ -423,7 +430,9 @@ def run_ours(args, cfg, rank, world, dist):
         "dtype": "e4m3 experts, bf16 elsewhere" if f8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
         "config": {**workload_config(cfg),
-                   "expert_gemm": "single-SM" if args.no_sm_pairs else "SM pairs where shapes allow"},
+                   "expert_gemm": "single-SM" if args.no_sm_pairs else "SM pairs where shapes allow",
+                   **({"capacity": args.capacity, "group_size": args.group_size,
+                       "rounds": rounds_info} if args.capacity > 0 else {})},
         "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
         "tc_roofline_frac": tc_ms / ms_step,
         "layer_roofline": {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms,
@@ -461,6 +470,13 @@ def main():
                     help="FP8 E4M3 expert GEMMs with delayed scaling")
     ap.add_argument("--no-sm-pairs", action="store_true",
                     help="expert GEMMs on single SMs instead of SM pairs (comparison runs)")
+    ap.add_argument("--capacity", type=int, default=0,
+                    help="multi-round fixed-capacity schedule: slots per expert per round "
+                         "(0: one dropless pass)")
+    ap.add_argument("--group-size", type=int, default=8,
+                    help="experts per borrowing group for --capacity")
+    ap.add_argument("--max-rounds", type=int, default=0,
+                    help="rounds launched per forward for --capacity (0: worst case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

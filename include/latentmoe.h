@@ -104,7 +104,9 @@ enum {
 /* Device status bits returned by latentmoe_get_status. */
 enum {
   LATENTMOE_STATUS_TIMEOUT = 1u,    /* a pipeline wait in a GEMM kernel gave up */
-  LATENTMOE_STATUS_BAD_EXPERT = 2u  /* an expert id outside [0, E) reached the sort */
+  LATENTMOE_STATUS_BAD_EXPERT = 2u, /* an expert id outside [0, E) reached the sort */
+  LATENTMOE_STATUS_ROUNDS = 4u      /* the capacity schedule needed more rounds than
+                                       max_rounds; the slots left over were not computed */
 };
 
 /* FP8 E4M3 expert GEMMs (LATENTMOE_FP8_EXPERTS). "The Training and RL
@@ -290,6 +292,35 @@ int latentmoe_set_profiling(latentmoe_t h, int slots);
 int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count);
 int latentmoe_num_stages(void);
 const char* latentmoe_stage_name(int stage);
+
+/* Multi-round fixed-capacity schedule of the expert GEMMs ("Frontier
+ * Pre-training at Microsoft AI", section "Dropless MoE with tunable,
+ * fixed-size memory usage"). Experts form groups of group_size consecutive
+ * experts (the last may be smaller). In every round each expert first runs
+ * up to `capacity` of its remaining slots; the group's unused capacity is
+ * then lent to experts with slots left, lowest expert index first; an
+ * expert's slots run in slot order across rounds. The rounds repeat until no
+ * slot is left (the count is the same for every group), so nothing is
+ * dropped and the output equals the one-pass forward. The expert hidden
+ * activations h live in a fixed buffer of E * capacity rows instead of one
+ * row per slot.
+ * max_rounds bounds the rounds launched per forward (each launches the two
+ * expert GEMMs; rounds without slots end at once); 0 chooses the worst case
+ * for max_tokens (every token putting min(k, group size) slots into the
+ * smallest group). Slots left after max_rounds are not computed and set
+ * LATENTMOE_STATUS_ROUNDS. capacity = 0 returns to the one-pass forward.
+ * Allocates the round buffer and the schedule arrays (synchronises the
+ * device). Errors: INVALID_ARG (negative values, group_size outside
+ * [1, E]), UNSUPPORTED (E * capacity > 2^30 rows, more than 4096 rounds),
+ * OUT_OF_MEMORY. */
+int latentmoe_set_capacity(latentmoe_t h, int64_t capacity, int64_t group_size,
+                           int64_t max_rounds);
+
+/* The last forward's round schedule (synchronises the device): info (host
+ * int32 [3]) = {rounds the routing needed, slots left over, rounds
+ * launched}; take (device int32 [rounds launched, E], may be NULL) = slots
+ * of each expert in each round. UNSUPPORTED when no capacity is set. */
+int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info);
 
 /* Expert GEMMs on SM pairs (enable = 1, the default) or on single SMs (0).
  * The pair kernels run tcgen05 MMAs with M = 256 over two SMs of a cluster,

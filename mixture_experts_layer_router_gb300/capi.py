@@ -32,6 +32,7 @@ FP8_TENSORS = 2  # scaled activations: z, h
 
 STATUS_TIMEOUT = 1
 STATUS_BAD_EXPERT = 2
+STATUS_ROUNDS = 4
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -70,6 +71,8 @@ SIGNATURES = {
     "latentmoe_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
     "latentmoe_get_launch_count": (ctypes.c_int, [_c_void_p, ctypes.POINTER(_i64)]),
     "latentmoe_set_sm_pairs": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
+    "latentmoe_set_capacity": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64]),
+    "latentmoe_get_rounds": (ctypes.c_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "latentmoe_last_cuda_error": (ctypes.c_int, [_c_void_p]),
     "latentmoe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "latentmoe_debug_gemm": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _i64, _i64,
@@ -296,6 +299,21 @@ class LatentMoE:
         check(load().latentmoe_get_fp8_weight_scales(self.handle, buf),
               "latentmoe_get_fp8_weight_scales")
         return [list(buf[m * E:(m + 1) * E]) for m in range(3)]
+
+    def set_capacity(self, capacity: int, group_size: int = 1, max_rounds: int = 0) -> None:
+        """Multi-round fixed-capacity expert schedule (capacity 0: one pass)."""
+        check(load().latentmoe_set_capacity(self.handle, capacity, group_size, max_rounds),
+              "latentmoe_set_capacity", self.handle)
+
+    def rounds(self, device="cuda"):
+        """{"needed", "left_over", "launched", "take" [launched, E] int32} of the last forward."""
+        import torch
+        info = (ctypes.c_int32 * 3)()
+        check(load().latentmoe_get_rounds(self.handle, None, info), "latentmoe_get_rounds")
+        take = torch.empty((info[2], self.dims.num_experts), dtype=torch.int32, device=device)
+        check(load().latentmoe_get_rounds(self.handle, take.data_ptr(), info),
+              "latentmoe_get_rounds")
+        return {"needed": info[0], "left_over": info[1], "launched": info[2], "take": take}
 
     def set_sm_pairs(self, enable: bool) -> None:
         check(load().latentmoe_set_sm_pairs(self.handle, int(enable)),

@@ -146,6 +146,16 @@ struct latentmoe {
   bool loaded = false;
   bool fp8 = false;             // E4M3 expert GEMMs
   bool sm_pairs = true;         // SM-pair grouped kernels where the shapes allow
+  // multi-round fixed-capacity expert schedule (capacity 0: one dropless pass)
+  int64_t cap = 0;
+  int cap_group = 0;
+  int cap_rounds = 0;
+  void* cap_mem = nullptr;      // round buffer of h, then the schedule arrays
+  void* hround = nullptr;       // [E * cap, F] bf16 or E4M3 codes
+  int* rin = nullptr;           // [cap_rounds, E]
+  int* rout = nullptr;          // [cap_rounds, E + 1]
+  int* rlen = nullptr;          // [cap_rounds, E]
+  int* rinfo = nullptr;         // {rounds used, slots left over}
   latentmoe_weights w;          // the library-owned copies below
   float* w_scale = nullptr;     // E4M3: [3E] scales of W_g, W_u, W_d per expert (in wmem)
   lmoe::Fp8State* f8 = nullptr; // E4M3: delayed-scaling state (in ws)
@@ -236,6 +246,104 @@ int run_routing(latentmoe* h, const float* logits, int T, cudaStream_t s, int sl
   const int r = run_sort(h, T, s);
   if (r != LATENTMOE_OK) return r;
   record(h, slot_base, 3, s);
+  return LATENTMOE_OK;
+}
+
+// One launch of the grouped gate+up GEMM over the groups described in `a`
+// (segments and output set by the caller): weights, scales and the kernel
+// (SM pairs where F % 256 == 0) from the handle.
+int launch_expert_gate_up(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok,
+                          cudaStream_t s) {
+  const int E = static_cast<int>(h->dims.num_experts);
+  const int l = static_cast<int>(h->dims.latent), F = static_cast<int>(h->dims.ffn);
+  a.num_groups = E;
+  a.fblocks = F / 128;
+  a.kb = l / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
+  a.w_group_rows = F;
+  a.n_out = F;
+  a.ldo = F;
+  a.status = h->status;
+  if (h->fp8) {
+    a.w_scale0 = h->w_scale;
+    a.w_scale1 = h->w_scale + E;
+    a.in_scale = &h->f8->scale[0];
+    a.out_scale = &h->f8->scale[1];
+    a.out_amax = &h->f8->amax[1];
+  }
+  if (h->sm_pairs && F % 256 == 0) {
+    a.fblocks = F / 256;
+    LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpSwiglu, h->fp8, tok, h->m_wg, h->m_wu, a,
+                                              h->sms, s));
+  } else {
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, h->fp8, tok, h->m_wg, h->m_wu, a,
+                                         h->sms, s));
+  }
+  h->launches += 1;
+  return LATENTMOE_OK;
+}
+
+// The same for the grouped down GEMM (SM pairs where l % 512 == 0).
+int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok, cudaStream_t s) {
+  const int E = static_cast<int>(h->dims.num_experts);
+  const int l = static_cast<int>(h->dims.latent), F = static_cast<int>(h->dims.ffn);
+  a.num_groups = E;
+  a.fblocks = ceil_div(l, 256);
+  a.kb = F / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
+  a.w_group_rows = l;
+  a.n_out = l;
+  a.ldo = l;
+  a.status = h->status;
+  a.w_scale0 = a.w_scale1 = a.in_scale = a.out_scale = nullptr;
+  a.out_amax = nullptr;
+  if (h->fp8) {
+    a.w_scale0 = a.w_scale1 = h->w_scale + 2 * E;
+    a.in_scale = &h->f8->scale[1];
+  }
+  if (h->sm_pairs && l % 512 == 0) {
+    a.fblocks = l / 512;
+    LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpPlain, h->fp8, tok, h->m_wd, h->m_wd, a,
+                                              h->sms, s));
+  } else {
+    LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, h->fp8, tok, h->m_wd, h->m_wd, a,
+                                         h->sms, s));
+  }
+  h->launches += 1;
+  return LATENTMOE_OK;
+}
+
+// Both expert GEMMs under the multi-round fixed-capacity schedule: the
+// schedule kernel, then per round r the gate+up of the round's slots (rows
+// rin of the expert-sorted z) into the round buffer (rows rout) and the down
+// GEMM from the round buffer back to the slots' rows of o. Rounds past the
+// ones the routing needs have no slots and end at once.
+int run_expert_rounds(latentmoe* h, const CUtensorMap& mzp, cudaStream_t s) {
+  const int E = static_cast<int>(h->dims.num_experts);
+  const int F = static_cast<int>(h->dims.ffn);
+  LMOE_CK(h, lmoe::launch_round_schedule(h->counts, h->offsets, E, static_cast<int>(h->cap),
+                                         h->cap_group, h->cap_rounds, h->rin, h->rout, h->rlen,
+                                         h->rinfo, h->status, s));
+  h->launches += 1;
+  CUtensorMap mhr;
+  if (!make_token_map(&mhr, h->hround, static_cast<uint64_t>(E) * h->cap, F, h->fp8))
+    return LATENTMOE_ERR_CUDA;
+  for (int r = 0; r < h->cap_rounds; ++r) {
+    lmoe::GroupedArgs a;
+    memset(&a, 0, sizeof(a));
+    a.seg_len = h->rlen + r * E;
+    a.in_start = h->rin + r * E;
+    a.out_start = h->rout + r * (E + 1);
+    a.out = h->hround;
+    int rc = launch_expert_gate_up(h, a, mzp, s);
+    if (rc != LATENTMOE_OK) return rc;
+    lmoe::GroupedArgs b;
+    memset(&b, 0, sizeof(b));
+    b.seg_len = h->rlen + r * E;
+    b.in_start = h->rout + r * (E + 1);
+    b.out_start = h->rin + r * E;
+    b.out = h->ob;
+    rc = launch_expert_down(h, b, mhr, s);
+    if (rc != LATENTMOE_OK) return rc;
+  }
   return LATENTMOE_OK;
 }
 
@@ -371,6 +479,7 @@ int latentmoe_destroy(latentmoe_t h) {
   if (h->y_stage) cudaFree(h->y_stage);
   if (h->ws) cudaFree(h->ws);
   if (h->wmem) cudaFree(h->wmem);
+  if (h->cap_mem) cudaFree(h->cap_mem);
   delete h;
   return LATENTMOE_OK;
 }
@@ -598,63 +707,25 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 4, s);
-  // 4: grouped gate+up with SwiGLU (weights on the M side, tokens on N)
-  {
+  if (h->cap > 0) {
+    // 4+5: multi-round fixed-capacity schedule: per round, gate+up of the
+    // round's slots into the fixed round buffer, then down back to the slots
+    const int r = run_expert_rounds(h, mzp, s);
+    if (r != LATENTMOE_OK) return r;
+    record(h, slot_base, 5, s);
+  } else {
+    // 4: grouped gate+up with SwiGLU (weights on the M side, tokens on N)
     lmoe::GroupedArgs a;
     memset(&a, 0, sizeof(a));
-    a.num_groups = E;
     a.seg_offsets = h->offsets;
-    a.fblocks = F / 128;
-    a.kb = l / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
-    a.w_group_rows = F;
-    a.n_out = F;
     a.out = h->hb;
-    a.ldo = F;
-    a.status = h->status;
-    if (h->fp8) {
-      a.w_scale0 = h->w_scale;
-      a.w_scale1 = h->w_scale + E;
-      a.in_scale = &h->f8->scale[0];
-      a.out_scale = &h->f8->scale[1];
-      a.out_amax = &h->f8->amax[1];
-    }
-    if (h->sm_pairs && F % 256 == 0) {
-      a.fblocks = F / 256;
-      LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu,
-                                                a, h->sms, s));
-    } else {
-      LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpSwiglu, h->fp8, mzp, h->m_wg, h->m_wu, a,
-                                           h->sms, s));
-    }
-    h->launches += 1;
-  }
-  record(h, slot_base, 5, s);
-  // 5: grouped expert down-projection
-  {
-    lmoe::GroupedArgs a;
-    memset(&a, 0, sizeof(a));
-    a.num_groups = E;
-    a.seg_offsets = h->offsets;
-    a.fblocks = ceil_div(l, 256);
-    a.kb = F / (h->fp8 ? lmoe::kGBK8 : lmoe::kGBK);
-    a.w_group_rows = l;
-    a.n_out = l;
+    int r = launch_expert_gate_up(h, a, mzp, s);
+    if (r != LATENTMOE_OK) return r;
+    record(h, slot_base, 5, s);
+    // 5: grouped expert down-projection
     a.out = h->ob;
-    a.ldo = l;
-    a.status = h->status;
-    if (h->fp8) {
-      a.w_scale0 = a.w_scale1 = h->w_scale + 2 * E;
-      a.in_scale = &h->f8->scale[1];
-    }
-    if (h->sm_pairs && l % 512 == 0) {
-      a.fblocks = l / 512;
-      LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd,
-                                                a, h->sms, s));
-    } else {
-      LMOE_CK(h, lmoe::launch_gemm_grouped(lmoe::kGrpPlain, h->fp8, mh, h->m_wd, h->m_wd, a,
-                                           h->sms, s));
-    }
-    h->launches += 1;
+    r = launch_expert_down(h, a, mh, s);
+    if (r != LATENTMOE_OK) return r;
   }
   record(h, slot_base, 6, s);
   // 6: combine
@@ -858,6 +929,82 @@ int latentmoe_get_stage_times(latentmoe_t h, int slot, float* ms, int count) {
     LMOE_CK(h, cudaEventElapsedTime(&t, h->events[base + i], h->events[base + i + 1]));
     ms[i] = t;
   }
+  return LATENTMOE_OK;
+}
+
+int latentmoe_set_capacity(latentmoe_t h, int64_t capacity, int64_t group_size,
+                           int64_t max_rounds) {
+  if (h == nullptr || capacity < 0 || max_rounds < 0) return LATENTMOE_ERR_INVALID_ARG;
+  const int64_t E = h->dims.num_experts, F = h->dims.ffn;
+  if (capacity > 0 && (group_size < 1 || group_size > E)) return LATENTMOE_ERR_INVALID_ARG;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  if (h->cap_mem) {
+    cudaFree(h->cap_mem);
+    h->cap_mem = nullptr;
+  }
+  h->cap = 0;
+  h->cap_group = 0;
+  h->cap_rounds = 0;
+  h->hround = nullptr;
+  h->rin = h->rout = h->rlen = h->rinfo = nullptr;
+  if (capacity == 0) return LATENTMOE_OK;
+  if (capacity * E > (1ll << 30)) return LATENTMOE_ERR_UNSUPPORTED;
+  int64_t rounds = max_rounds;
+  if (rounds == 0) {
+    // worst case: every token puts min(k, g) of its slots into the smallest group
+    const int64_t gmin = E % group_size ? E % group_size : group_size;
+    const int64_t per = h->dims.max_tokens * (h->k < gmin ? h->k : gmin);
+    rounds = (per + gmin * capacity - 1) / (gmin * capacity);
+    if (rounds < 1) rounds = 1;
+  }
+  if (rounds > 4096) return LATENTMOE_ERR_UNSUPPORTED;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 1024);
+    return o;
+  };
+  const size_t o_h = take(static_cast<size_t>(E * capacity) * F * (h->fp8 ? 1 : 2));
+  const size_t o_in = take(static_cast<size_t>(rounds * E) * 4);
+  const size_t o_out = take(static_cast<size_t>(rounds * (E + 1)) * 4);
+  const size_t o_len = take(static_cast<size_t>(rounds * E) * 4);
+  const size_t o_info = take(16);
+  {
+    const cudaError_t e = cudaMalloc(&h->cap_mem, off);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->cap_mem = nullptr;
+      return fail_cuda(h, e);
+    }
+  }
+  char* base = static_cast<char*>(h->cap_mem);
+  h->hround = base + o_h;
+  h->rin = reinterpret_cast<int*>(base + o_in);
+  h->rout = reinterpret_cast<int*>(base + o_out);
+  h->rlen = reinterpret_cast<int*>(base + o_len);
+  h->rinfo = reinterpret_cast<int*>(base + o_info);
+  LMOE_CK(h, cudaMemset(h->rinfo, 0, 16));
+  h->cap = capacity;
+  h->cap_group = static_cast<int>(group_size);
+  h->cap_rounds = static_cast<int>(rounds);
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info) {
+  if (h == nullptr || info == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (h->cap == 0) return LATENTMOE_ERR_UNSUPPORTED;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  LMOE_CK(h, cudaDeviceSynchronize());
+  int32_t v[2];
+  LMOE_CK(h, cudaMemcpy(v, h->rinfo, 8, cudaMemcpyDeviceToHost));
+  info[0] = v[0];
+  info[1] = v[1];
+  info[2] = h->cap_rounds;
+  if (take)
+    LMOE_CK(h, cudaMemcpy(take, h->rlen,
+                          static_cast<size_t>(h->cap_rounds) * h->dims.num_experts * 4,
+                          cudaMemcpyDeviceToDevice));
   return LATENTMOE_OK;
 }
 

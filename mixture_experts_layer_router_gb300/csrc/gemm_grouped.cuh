@@ -65,12 +65,18 @@ constexpr int kGBarrierBytes = 8 * (2 * kGStages + 3);
 constexpr int kGStagePitch = 80;              // 64 B of bf16 + 16 B pad per token row
 constexpr int kGStageWarpBytes = 32 * kGStagePitch;
 constexpr int kGMaxGroups = 512;
-constexpr int kGSmemBytes = 1024 + kGStages * kGStageBytes + kGBarrierBytes + 16 +
-                            2 * (kGMaxGroups + 1) * 4 + kGEpiWarps * kGStageWarpBytes;
+// group table: first input row, first output row, rows, tile prefix
+constexpr int kGTableBytes = (4 * kGMaxGroups + 1) * 4;
+constexpr int kGSmemBytes = 1024 + kGStages * kGStageBytes + kGBarrierBytes + 16 + kGTableBytes +
+                            16 /* staging alignment */ + kGEpiWarps * kGStageWarpBytes;
 
 struct GroupedArgs {
   int num_groups;          // G <= kGMaxGroups
-  const int* seg_offsets;  // [G+1] token row offsets of the groups
+  const int* seg_offsets;  // [G+1] row offsets of the groups (input rows = output rows),
+                           // used when seg_len is null
+  const int* seg_len;      // [G] rows of each group, or null
+  const int* in_start;     // [G] first token row of each group (with seg_len)
+  const int* out_start;    // [G] first output row of each group (with seg_len)
   int fblocks;             // feature blocks per group (SwiGLU: F/128; plain: ceil(N/256))
   int kb;                  // k-blocks (K / 64)
   int w_group_rows;        // weight rows per group in the weight maps
@@ -89,6 +95,7 @@ struct GroupedArgs {
 struct GTile {
   int g;      // group
   int tok0;   // first token row
+  int out0;   // first output row
   int len;    // valid tokens (<= 256)
   int n;      // MMA N: len rounded up to 16
   int f;      // feature block
@@ -101,24 +108,91 @@ __device__ __forceinline__ void group_chunks(int n, int& nch, int& cs) {
   cs = (per + 15) & ~15;
 }
 
-template <int MODE>
-__device__ __forceinline__ GTile decode_gtile(int t, const GroupedArgs& a, const int* seg_s,
-                                              const int* tp_s) {
+// Group table in shared memory (kGTableBytes): per group its first input
+// row, first output row and row count, then the exclusive prefix of tiles.
+struct GroupTable {
+  int* in;
+  int* out;
+  int* len;
+  int* tp;
+};
+
+// The epilogue staging rows start on the next 16-byte boundary after the table.
+__device__ __forceinline__ uint8_t* staging_after_table(void* table) {
+  const uintptr_t p = reinterpret_cast<uintptr_t>(table) + kGTableBytes;
+  return reinterpret_cast<uint8_t*>((p + 15) & ~static_cast<uintptr_t>(15));
+}
+
+__device__ __forceinline__ GroupTable group_table_at(void* p) {
+  int* b = static_cast<int*>(p);
+  return GroupTable{b, b + kGMaxGroups, b + 2 * kGMaxGroups, b + 3 * kGMaxGroups};
+}
+
+__device__ __forceinline__ void load_group_table(const GroupedArgs& a, const GroupTable& gt) {
+  for (int i = threadIdx.x; i < a.num_groups; i += blockDim.x) {
+    if (a.seg_len != nullptr) {
+      gt.in[i] = a.in_start[i];
+      gt.out[i] = a.out_start[i];
+      gt.len[i] = a.seg_len[i];
+    } else {
+      const int s0 = a.seg_offsets[i];
+      gt.in[i] = s0;
+      gt.out[i] = s0;
+      gt.len[i] = a.seg_offsets[i + 1] - s0;
+    }
+  }
+}
+
+// Exclusive prefix over groups of (token chunks x tiles per chunk), by one warp.
+__device__ __forceinline__ void build_tile_prefix(const GroupedArgs& a, const GroupTable& gt,
+                                                  int tiles_per_chunk) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  if (lane == 0) gt.tp[0] = 0;
+  for (int base = 0; base < a.num_groups; base += 32) {
+    const int g = base + lane;
+    int v = 0;
+    if (g < a.num_groups) {
+      const int n = gt.len[g];
+      if (n > 0) {
+        int nch, cs;
+        group_chunks(n, nch, cs);
+        v = nch * tiles_per_chunk;
+      }
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += o;
+    }
+    if (g < a.num_groups) gt.tp[g + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+// The group of tile t: the largest g with tp[g] <= t (that group is non-empty).
+__device__ __forceinline__ int tile_group(int t, const GroupedArgs& a, const GroupTable& gt) {
   int lo = 0, hi = a.num_groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (tp_s[mid] <= t) lo = mid; else hi = mid - 1;
+    if (gt.tp[mid] <= t) lo = mid; else hi = mid - 1;
   }
-  const int g = lo;
-  const int n = seg_s[g + 1] - seg_s[g];
+  return lo;
+}
+
+template <int MODE>
+__device__ __forceinline__ GTile decode_gtile(int t, const GroupedArgs& a, const GroupTable& gt) {
+  const int g = tile_group(t, a, gt);
+  const int n = gt.len[g];
   int nch, cs;
   group_chunks(n, nch, cs);
-  const int local = t - tp_s[g];
+  const int local = t - gt.tp[g];
   const int f = local / nch;
   const int c = local - f * nch;
   GTile r;
   r.g = g;
-  r.tok0 = seg_s[g] + c * cs;
+  r.tok0 = gt.in[g] + c * cs;
+  r.out0 = gt.out[g] + c * cs;
   r.len = min(cs, n - c * cs);
   r.n = (r.len + 15) & ~15;
   r.f = f;
@@ -202,9 +276,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint64_t* done_bar = tempty_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
-  int* tp_s = seg_s + kGMaxGroups + 1;
-  uint8_t* stage_smem = reinterpret_cast<uint8_t*>(tp_s + kGMaxGroups + 1);
+  const GroupTable gt = group_table_at(tmem_slot + 4);
+  uint8_t* stage_smem = staging_after_table(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -230,38 +303,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
+  load_group_table(a, gt);
   __syncthreads();
-  if (warp == 2) {
-    // exclusive prefix over groups of (token chunks x feature blocks)
-    int carry = 0;
-    if (lane == 0) tp_s[0] = 0;
-    for (int base = 0; base < a.num_groups; base += 32) {
-      const int g = base + lane;
-      int v = 0;
-      if (g < a.num_groups) {
-        const int n = seg_s[g + 1] - seg_s[g];
-        if (n > 0) {
-          int nch, cs;
-          group_chunks(n, nch, cs);
-          v = nch * a.fblocks;
-        }
-      }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
-      }
-      if (g < a.num_groups) tp_s[g + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
+  if (warp == 2) build_tile_prefix(a, gt, a.fblocks);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
 
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = tp_s[a.num_groups];
+  const int total_tiles = gt.tp[a.num_groups];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -275,7 +325,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+        const GTile c = decode_gtile<MODE>(t, a, gt);
         const bool two = second_acc_used<MODE>(a, c.f);
         const int nbox = (c.n + kGTokBox - 1) / kGTokBox;
         const uint32_t bytes = kGWeightTile * (two ? 2 : 1) + nbox * kGTokBoxBytes;
@@ -318,7 +368,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+        const GTile c = decode_gtile<MODE>(t, a, gt);
         const bool two = second_acc_used<MODE>(a, c.f);
         const uint32_t idesc = F8 ? instr_desc_e4m3(128, c.n) : instr_desc_bf16(128, c.n);
         if (!wait_bounded(tempty_bar, acc_phase ^ 1u, abort_flag, a.status)) break;
@@ -369,7 +419,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const float out_inv = (F8 && MODE == kGrpSwiglu) ? inv_scale(*a.out_scale) : 1.0f;
     float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const GTile c = decode_gtile<MODE>(t, a, seg_s, tp_s);
+      const GTile c = decode_gtile<MODE>(t, a, gt);
       const bool two = second_acc_used<MODE>(a, c.f);
       if (!warp_wait_bounded(tfull_bar, acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
@@ -407,7 +457,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const int ch = half + 2 * i;
           if (ch < nchunks)
-            gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+            gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
                             c.len - ch * 32, feat0);
         }
       } else if constexpr (MODE == kGrpSwiglu) {
@@ -437,12 +487,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const int ch = half + 2 * i;
           if (ch < nchunks)
-            gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+            gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
                          c.len - ch * 32, feat0);
         }
       } else {
         for (int ch = half; ch < nchunks; ch += 2) {
-          const long long tok_row0 = static_cast<long long>(c.tok0) + ch * 32;
+          const long long tok_row0 = static_cast<long long>(c.out0) + ch * 32;
           const int tok_valid = c.len - ch * 32;
 #pragma unroll 1
           for (int acc = 0; acc < 2; ++acc) {

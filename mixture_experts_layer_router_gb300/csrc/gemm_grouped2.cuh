@@ -35,35 +35,31 @@ constexpr int kPStages = 4;
 constexpr int kPTokenTile = 128 * 128;  // up to 128 token rows of 128 bytes
 constexpr int kPStageBytes = 2 * kGWeightTile + kPTokenTile;  // 48 KB
 constexpr int kPBarrierBytes = 8 * (2 * kPStages + 3);
-constexpr int kPSmemBytes = 1024 + kPStages * kPStageBytes + kPBarrierBytes + 16 +
-                            2 * (kGMaxGroups + 1) * 4 + kGEpiWarps * kGStageWarpBytes;
+constexpr int kPSmemBytes = 1024 + kPStages * kPStageBytes + kPBarrierBytes + 16 + kGTableBytes +
+                            16 /* staging alignment */ + kGEpiWarps * kGStageWarpBytes;
 static_assert(kPSmemBytes <= 232448, "pair kernel shared memory");
 
 struct PTile {
   int g;      // group
   int tok0;   // first token row of the chunk
+  int out0;   // first output row of the chunk
   int len;    // valid tokens (<= 256)
   int n;      // MMA N: len rounded up to 16
   int p;      // pair feature block
 };
 
-__device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const int* seg_s,
-                                              const int* tp_s) {
-  int lo = 0, hi = a.num_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tp_s[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  const int g = lo;
-  const int n = seg_s[g + 1] - seg_s[g];
+__device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const GroupTable& gt) {
+  const int g = tile_group(t, a, gt);
+  const int n = gt.len[g];
   int nch, cs;
   group_chunks(n, nch, cs);
-  const int local = t - tp_s[g];
+  const int local = t - gt.tp[g];
   const int p = local / nch;
   const int c = local - p * nch;
   PTile r;
   r.g = g;
-  r.tok0 = seg_s[g] + c * cs;
+  r.tok0 = gt.in[g] + c * cs;
+  r.out0 = gt.out[g] + c * cs;
   r.len = min(cs, n - c * cs);
   r.n = (r.len + 15) & ~15;
   r.p = p;
@@ -87,9 +83,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint64_t* done_bar = tempty_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* seg_s = reinterpret_cast<int*>(tmem_slot + 4);
-  int* tp_s = seg_s + kGMaxGroups + 1;
-  uint8_t* stage_smem = reinterpret_cast<uint8_t*>(tp_s + kGMaxGroups + 1);
+  const GroupTable gt = group_table_at(tmem_slot + 4);
+  uint8_t* stage_smem = staging_after_table(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -121,32 +116,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tmem_alloc_pair(tmem_slot, 512);
     tmem_relinquish_pair();
   }
-  for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
+  load_group_table(a, gt);
   __syncthreads();
-  if (warp == 2) {
-    // exclusive prefix over groups of (token chunks x pair feature blocks)
-    int carry = 0;
-    if (lane == 0) tp_s[0] = 0;
-    for (int base = 0; base < a.num_groups; base += 32) {
-      const int g = base + lane;
-      int v = 0;
-      if (g < a.num_groups) {
-        const int n = seg_s[g + 1] - seg_s[g];
-        if (n > 0) {
-          int nch, cs;
-          group_chunks(n, nch, cs);
-          v = nch * a.fblocks;
-        }
-      }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
-      }
-      if (g < a.num_groups) tp_s[g + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
+  if (warp == 2) build_tile_prefix(a, gt, a.fblocks);
   tc_fence_before_sync();
   __syncthreads();
   // both CTAs' barriers are initialised before either touches the other's
@@ -154,7 +126,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after_sync();
 
   const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = tp_s[a.num_groups];
+  const int total_tiles = gt.tp[a.num_groups];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -166,7 +138,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int t = pair; t < total_tiles && ok; t += npairs) {
-        const PTile c = decode_ptile(t, a, seg_s, tp_s);
+        const PTile c = decode_ptile(t, a, gt);
         const int half = c.n >> 1;
         const int nbox = (half + kGTokBox - 1) / kGTokBox;
         const uint32_t bytes = 2u * (2 * kGWeightTile + nbox * kGTokBoxBytes);
@@ -217,7 +189,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < total_tiles && ok; t += npairs) {
-        const PTile c = decode_ptile(t, a, seg_s, tp_s);
+        const PTile c = decode_ptile(t, a, gt);
         const uint32_t idesc = F8 ? instr_desc_e4m3(256, c.n) : instr_desc_bf16(256, c.n);
         if (!wait_bounded_pair(tempty_bar, acc_phase ^ 1u, abort_flag, peer_abort, a.status))
           break;
@@ -268,7 +240,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const float out_inv = (F8 && MODE == kGrpSwiglu) ? inv_scale(*a.out_scale) : 1.0f;
     float amax = 0.0f;
     for (int t = pair; t < total_tiles; t += npairs) {
-      const PTile c = decode_ptile(t, a, seg_s, tp_s);
+      const PTile c = decode_ptile(t, a, gt);
       if (!warp_wait_bounded_pair(tfull_bar, acc_phase, abort_flag, peer_abort, a.status)) break;
       tc_fence_after_sync();
       const int nchunks = (c.len + 31) / 32;
@@ -306,7 +278,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           for (int i = 0; i < 4; ++i) {
             const int ch = half + 2 * i;
             if (ch < nchunks)
-              gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+              gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
                               c.len - ch * 32, feat0);
           }
         } else {
@@ -333,14 +305,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
           for (int i = 0; i < 4; ++i) {
             const int ch = half + 2 * i;
             if (ch < nchunks)
-              gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.tok0) + ch * 32,
+              gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
                            c.len - ch * 32, feat0);
           }
         }
       } else {
         const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
         for (int ch = half; ch < nchunks; ch += 2) {
-          const long long tok_row0 = static_cast<long long>(c.tok0) + ch * 32;
+          const long long tok_row0 = static_cast<long long>(c.out0) + ch * 32;
           const int tok_valid = c.len - ch * 32;
 #pragma unroll 1
           for (int acc = 0; acc < 2; ++acc) {

@@ -108,6 +108,16 @@ cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbas
                         int* offsets, int* perm, int* pos, unsigned* status, cudaStream_t s);
 constexpr int kSortLaunches = 3;
 
+// Multi-round fixed-capacity schedule (capacity C per expert per round,
+// groups of G consecutive experts, at most max_rounds rounds): per round r,
+// rlen[r*E+e] slots of expert e starting at row rin[r*E+e] of the
+// expert-sorted slots, placed at row rout[r*(E+1)+e] of the round buffer
+// (rout[r*(E+1)+E] = the round's total); info = {rounds used, slots left
+// over}. Slots left over set kStatusRounds. One launch of one block.
+cudaError_t launch_round_schedule(const int* counts, const int* offsets, int E, int C, int G,
+                                  int max_rounds, int* rin, int* rout, int* rlen, int* info,
+                                  unsigned* status, cudaStream_t s);
+
 // c[t] = sum_j gates[t,j] * o[pos[t,j]] in fp32, j order; bf16 out.
 cudaError_t launch_combine(const __nv_bfloat16* o, const float* gates, const int* pos, int T,
                            int k, int l, __nv_bfloat16* c, cudaStream_t s);

@@ -16,6 +16,7 @@ namespace lmoe {
 
 constexpr unsigned kStatusTimeout = 1u;    // LATENTMOE_STATUS_TIMEOUT
 constexpr unsigned kStatusBadExpert = 2u;  // LATENTMOE_STATUS_BAD_EXPERT
+constexpr unsigned kStatusRounds = 4u;     // LATENTMOE_STATUS_ROUNDS
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
