@@ -18,6 +18,11 @@ module restates that for the two expert GEMMs of the layer:
   the ones it used).
 - g = (q_z q_g^T) s_z s_g, u = (q_z q_u^T) s_z s_u, h = SiLU(g) u,
   o = (q_h q_d^T) s_h s_d.
+- With the dense GEMMs in E4M3 too (forward_fp8's ``dense``): x, the
+  combined latent c and the shared expert's hidden are quantized with their
+  own per-tensor scales, and the latent projections and the shared expert's
+  weights with one scale per matrix; the router keeps fp32 logits (the
+  pages keep routing in FP32).
 
 Readings where the pages are silent: scales are per tensor, and per expert
 for the expert weights; the history starts empty and a scale of 1 is used
@@ -117,7 +122,8 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
                 renorm: bool = False, logits: Optional[np.ndarray] = None,
                 z_codes: Optional[np.ndarray] = None,
                 h_codes: Optional[np.ndarray] = None,
-                wq_cache: Optional[dict] = None) -> Dict[str, np.ndarray]:
+                wq_cache: Optional[dict] = None,
+                dense: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """The layer with FP8 E4M3 expert GEMMs; everything else as ref.forward.
 
     z_codes [T*k, l] / h_codes [T*k, F] (E4M3 code values, slot order), when
@@ -125,7 +131,15 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
     expert GEMMs are then evaluated on exactly those codes. The returned
     "z_q" and "h_q" are the codes used, and "h" the unquantized h.
     wq_cache, a dict kept by the caller, holds each expert's quantized
-    weights across calls on the same weights."""
+    weights across calls on the same weights.
+
+    dense, when given, runs the other forward GEMMs in E4M3 as well (the
+    router keeps its fp32 logits): {"s_x", "s_c", "s_sh"} are the scales of
+    x, of the combined latent c and of the shared expert's hidden SiLU(g)*u;
+    optional "x_codes" [T, d], "c_codes" [T, l], "sh_codes" [T, F_s] replace
+    the codes formed here. Then z = s_x s_dn (x_q W_dn_q^T), y = s_c s_up
+    (c_q W_up_q^T) + s_sh s_ds (sh_q W_ds_q^T) with sh from s_x-scaled
+    products of x_q and the shared weights' codes."""
     x = np.asarray(x, dtype=np.float64)
     E = weights.num_experts
     L = ref.router_logits(x, weights.w_r, weights.b_r) if logits is None else \
@@ -133,7 +147,16 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
     p = ref.softmax_rows(L)
     idx = ref.top_k_stable(L, k)
     g = ref.select_gates(p, idx, renorm)
-    z = ref.latent_down(x, weights.w_dn)
+    out = {}
+    if dense is None:
+        z = ref.latent_down(x, weights.w_dn)
+    else:
+        s_x = dense["s_x"]
+        xq = quantize_act(x, s_x) if dense.get("x_codes") is None else \
+            np.asarray(dense["x_codes"], dtype=np.float64)
+        qdn, sdn = quantize_weight(weights.w_dn)
+        z = (xq @ qdn.T) * (s_x * sdn)
+        out.update({"x_q": xq, "x_amax": float(np.abs(x).max()) if x.size else 0.0, "z": z})
     counts, offsets, perm, pos = ref.counting_sort(idx, E)
     zq_slots = quantize_act(z, s_z)[perm] if z_codes is None else \
         np.asarray(z_codes, dtype=np.float64)
@@ -167,11 +190,29 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         hq_all[lo:hi] = qh
         H[lo:hi] = (qh @ qd.T) * (s_h * sd)
     c = ref.combine(H, g, pos)
-    y = ref.latent_up(c, weights.w_up)
-    if weights.w_gs is not None:
-        y = y + ref.shared_expert(x, weights.w_gs, weights.w_us, weights.w_ds)
+    if dense is None:
+        y = ref.latent_up(c, weights.w_up)
+        if weights.w_gs is not None:
+            y = y + ref.shared_expert(x, weights.w_gs, weights.w_us, weights.w_ds)
+    else:
+        s_c, s_sh = dense["s_c"], dense["s_sh"]
+        cq = quantize_act(c, s_c) if dense.get("c_codes") is None else \
+            np.asarray(dense["c_codes"], dtype=np.float64)
+        qup, sup = quantize_weight(weights.w_up)
+        y = (cq @ qup.T) * (s_c * sup)
+        out.update({"c": c, "c_q": cq, "c_amax": float(np.abs(c).max()) if c.size else 0.0})
+        if weights.w_gs is not None:
+            qgs, sgs = quantize_weight(weights.w_gs)
+            qus, sus = quantize_weight(weights.w_us)
+            qds, sds = quantize_weight(weights.w_ds)
+            sh = ref.silu((xq @ qgs.T) * (s_x * sgs)) * ((xq @ qus.T) * (s_x * sus))
+            shq = quantize_act(sh, s_sh) if dense.get("sh_codes") is None else \
+                np.asarray(dense["sh_codes"], dtype=np.float64)
+            y = y + (shq @ qds.T) * (s_sh * sds)
+            out.update({"sh": sh, "sh_q": shq, "sh_amax": float(np.abs(sh).max())})
     # the maxima delayed scaling records for the next step's scales
     z_amax = float(np.abs(z).max()) if z.size else 0.0
-    return {"idx": idx, "gates": g, "counts": counts, "offsets": offsets, "pos": pos,
-            "perm": perm, "y": y, "z_amax": z_amax, "h_amax": h_amax, "z_q": zq_slots,
-            "h": h_all, "h_q": hq_all}
+    out.update({"idx": idx, "gates": g, "counts": counts, "offsets": offsets, "pos": pos,
+                "perm": perm, "y": y, "z_amax": z_amax, "h_amax": h_amax, "z_q": zq_slots,
+                "h": h_all, "h_q": hq_all})
+    return out

@@ -237,3 +237,73 @@ def test_weight_cache_changes_nothing():
     b = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, wq_cache=cache)
     c = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, wq_cache=cache)
     assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["y"], c["y"]) and cache
+
+
+def _grid_layer_dense(seed, T=24, d=32, l=16, E=4, k=2, F=24, Fs=40):
+    """Like _grid_layer, with the dense weights on E4M3 grids too (power-of-
+    two scales): x, W_dn, W_up and the shared weights quantize exactly."""
+    rng = np.random.default_rng(seed)
+    v = fp8.e4m3_values()
+    codes = lambda shape: rng.choice(np.concatenate([v, -v]), size=shape)
+
+    def with_max(shape, e2):
+        c = codes(shape)
+        c.flat[rng.integers(c.size)] = 448.0
+        return c * 2.0 ** e2
+    sx = 2.0 ** -8
+    w = {
+        "x": codes((T, d)) * sx,
+        "w_r": rng.standard_normal((E, d)),
+        "w_dn": with_max((l, d), -12), "w_up": with_max((d, l), -11),
+        "w_g": np.stack([with_max((F, l), -(9 + e)) for e in range(E)]),
+        "w_u": np.stack([with_max((F, l), -(10 + e)) for e in range(E)]),
+        "w_d": np.stack([with_max((l, F), -(10 + e)) for e in range(E)]),
+        "w_gs": with_max((Fs, d), -12), "w_us": with_max((Fs, d), -11),
+        "w_ds": with_max((d, Fs), -12),
+    }
+    W = ref.OracleWeights.from_stacked(w["w_r"], w["w_dn"], w["w_up"], w["w_g"], w["w_u"],
+                                       w["w_d"], w_gs=w["w_gs"], w_us=w["w_us"], w_ds=w["w_ds"])
+    return w, W, sx
+
+
+def test_dense_e4m3_error_is_the_rounding_of_c_and_sh():
+    """Exact x and dense weights: the dense E4M3 layer differs from the
+    expert-only E4M3 layer (same z and h codes) only by the rounding of c
+    and of the shared hidden, each bounded elementwise by its half-step."""
+    w, W, sx = _grid_layer_dense(11)
+    k = 2
+    base = fp8.forward_fp8(w["x"], W, k, s_z=1.0, s_h=1.0)
+    s_z, s_h = base["z_amax"] / 448, base["h_amax"] / 448
+    experts = fp8.forward_fp8(w["x"], W, k, s_z=s_z, s_h=s_h)
+    probe = fp8.forward_fp8(w["x"], W, k, s_z=s_z, s_h=s_h,
+                            dense={"s_x": sx, "s_c": 1.0, "s_sh": 1.0})
+    s_c, s_sh = probe["c_amax"] / 448, probe["sh_amax"] / 448
+    got = fp8.forward_fp8(w["x"], W, k, s_z=s_z, s_h=s_h,
+                          dense={"s_x": sx, "s_c": s_c, "s_sh": s_sh})
+    assert np.array_equal(got["x_q"] * sx, w["x"])             # x exact on its grid
+    assert np.array_equal(got["z_q"], experts["z_q"])          # so z and h codes agree
+    assert np.array_equal(got["h_q"], experts["h_q"])
+    shared = ref.shared_expert(w["x"], w["w_gs"], w["w_us"], w["w_ds"])
+    y_exp_noshared = experts["y"] - shared
+    c, sh = got["c"], got["sh"]
+    hc = np.maximum(np.abs(c) * 2.0 ** -4, 2.0 ** -10 * s_c)
+    hs = np.maximum(np.abs(sh) * 2.0 ** -4, 2.0 ** -10 * s_sh)
+    bound = hc @ np.abs(w["w_up"]).T + hs @ np.abs(w["w_ds"]).T
+    err = np.abs(got["y"] - (y_exp_noshared + shared))
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-300) and err.max() > 0
+    # the maxima the dense path records
+    assert got["x_amax"] == np.abs(w["x"]).max()
+    assert got["c_amax"] == np.abs(c).max() and got["sh_amax"] == np.abs(sh).max()
+
+
+def test_dense_given_codes_reproduce_own_codes():
+    w, W, sx = _grid_layer_dense(12)
+    d = {"s_x": sx * 3, "s_c": 0.01, "s_sh": 0.02}
+    a = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, dense=d)
+    b = fp8.forward_fp8(w["x"], W, 2, s_z=0.01, s_h=0.003, z_codes=a["z_q"], h_codes=a["h_q"],
+                        dense={**d, "x_codes": a["x_q"], "c_codes": a["c_q"],
+                               "sh_codes": a["sh_q"]})
+    assert np.array_equal(a["y"], b["y"])
+
+
+FP8_CHECKS += [test_dense_e4m3_error_is_the_rounding_of_c_and_sh]
