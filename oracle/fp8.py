@@ -112,6 +112,13 @@ def quantize_weight(w: np.ndarray):
     return round_e4m3(prod), s
 
 
+def quantize_input(t: np.ndarray, s: float) -> np.ndarray:
+    """Codes of a tensor given in bf16 (exact in fp32) with scale s, the
+    product taken in fp32 as the kernel does: E4M3(fp32(t) * fp32(1/s))."""
+    inv = np.float32(1.0) / np.float32(s)
+    return round_e4m3((np.asarray(t, dtype=np.float32) * inv).astype(np.float64))
+
+
 def quantize_act(t: np.ndarray, s: float) -> np.ndarray:
     """Activation codes E4M3(t * (1/s)); t is the float64 oracle value."""
     inv = float(np.float32(1.0) / np.float32(s))
@@ -152,7 +159,9 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
         z = ref.latent_down(x, weights.w_dn)
     else:
         s_x = dense["s_x"]
-        xq = quantize_act(x, s_x) if dense.get("x_codes") is None else \
+        # x is given in bf16: its codes are decided from the fp32 product, as
+        # in the kernel, so both sides start from the same codes
+        xq = quantize_input(x, s_x) if dense.get("x_codes") is None else \
             np.asarray(dense["x_codes"], dtype=np.float64)
         qdn, sdn = quantize_weight(weights.w_dn)
         z = (xq @ qdn.T) * (s_x * sdn)
@@ -214,5 +223,5 @@ def forward_fp8(x: np.ndarray, weights: ref.OracleWeights, k: int, s_z: float, s
     z_amax = float(np.abs(z).max()) if z.size else 0.0
     out.update({"idx": idx, "gates": g, "counts": counts, "offsets": offsets, "pos": pos,
                 "perm": perm, "y": y, "z_amax": z_amax, "h_amax": h_amax, "z_q": zq_slots,
-                "h": h_all, "h_q": hq_all})
+                "h": h_all, "h_q": hq_all, "o": H})
     return out

@@ -307,3 +307,15 @@ def test_dense_given_codes_reproduce_own_codes():
 
 
 FP8_CHECKS += [test_dense_e4m3_error_is_the_rounding_of_c_and_sh]
+
+
+def test_quantize_input_matches_act_when_the_product_is_exact():
+    """bf16 values times a power-of-two reciprocal: the fp32 product is exact,
+    so the fp32 and float64 decisions agree everywhere; with a general scale
+    they differ only where the fp32 product lands on the other side of a
+    midpoint."""
+    rng = np.random.default_rng(3)
+    t = np.asarray(torch.from_numpy(rng.standard_normal(5000)).to(torch.bfloat16).double())
+    assert np.array_equal(fp8.quantize_input(t, 2.0 ** -5), fp8.quantize_act(t, 2.0 ** -5))
+    a, b = fp8.quantize_input(t, 0.0137), fp8.quantize_act(t, 0.0137)
+    assert (a != b).mean() < 1e-2
