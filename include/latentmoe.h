@@ -86,8 +86,11 @@ enum {
                                  and RL Infrastructure Behind MAI-Thinking-1",
                                  section "Sharding and parallelism". Not together
                                  with LATENTMOE_ROUTER_BIAS. */
-  LATENTMOE_FP8_EXPERTS = 16u /* the expert GEMMs in FP8 E4M3 with delayed
-                                 scaling; see "FP8 E4M3 expert GEMMs" below */
+  LATENTMOE_FP8_EXPERTS = 16u, /* the expert GEMMs in FP8 E4M3 with delayed
+                                  scaling; see "FP8 E4M3 GEMMs" below */
+  LATENTMOE_FP8_DENSE = 32u    /* with LATENTMOE_FP8_EXPERTS: the latent down-
+                                  and up-projections and the shared expert in
+                                  FP8 E4M3 as well (the router stays fp32) */
 };
 
 enum {
@@ -109,7 +112,7 @@ enum {
                                        max_rounds; the slots left over were not computed */
 };
 
-/* FP8 E4M3 expert GEMMs (LATENTMOE_FP8_EXPERTS). "The Training and RL
+/* FP8 E4M3 GEMMs (LATENTMOE_FP8_EXPERTS, LATENTMOE_FP8_DENSE). "The Training and RL
  * Infrastructure Behind MAI-Thinking-1", section "2. Numerics": forward
  * GEMMs in FP8 E4M3, per-tensor scales from a 1,024-step history of absolute
  * maxima (delayed scaling). E4M3 here: 4 exponent bits (bias 7), 3 mantissa
@@ -124,9 +127,16 @@ enum {
  *   kernel enters the maxima into a 1024-entry ring per tensor and sets
  *   s = max(ring) / 448 for the next forward (unchanged while the ring holds
  *   only zeros). A new handle starts with s = 1 and an empty ring.
- * - Everything else (router, down- and up-projection, shared expert,
- *   combine) is as without the flag. */
-#define LATENTMOE_FP8_TENSORS 2 /* scaled activations, in order: z, h */
+ * - With LATENTMOE_FP8_DENSE as well: W_dn, W_up and the shared expert's
+ *   W_gs, W_us, W_ds are quantized with one scale per matrix; x, the
+ *   combined latent c and the shared expert's hidden SiLU(x W_gs^T) *
+ *   (x W_us^T) get delayed per-tensor scales like z and h. The combine
+ *   still sums in fp32 and quantizes its result; the up-projection and the
+ *   shared expert's down-projection accumulate separately and are added in
+ *   fp32 before the output is rounded.
+ * - The router (fp32 logits from bf16 x and W_r) is never quantized; without
+ *   LATENTMOE_FP8_DENSE everything outside the expert GEMMs is bf16. */
+#define LATENTMOE_FP8_TENSORS 5 /* scaled activations, in order: z, h, x, c, shared hidden */
 
 /* Create a handle on the current device: validates dims, top_k (1..16,
  * <= E) and flags, and allocates the workspace for max_tokens tokens
@@ -259,13 +269,22 @@ int latentmoe_get_fp8_state(latentmoe_t h, float* scales, float* last_amax,
 int latentmoe_get_fp8_codes(latentmoe_t h, uint8_t* z_codes, uint8_t* h_codes,
                             latentmoe_stream_t stream);
 
+/* E4M3 codes of the last forward's x [T, d], c [T, l] and shared hidden
+ * [T, F_s] (LATENTMOE_FP8_DENSE), copied into caller device buffers on
+ * `stream`; any may be NULL (sh_codes must be NULL without a shared
+ * expert). UNSUPPORTED without LATENTMOE_FP8_DENSE, INVALID_ARG before the
+ * first forward. */
+int latentmoe_get_fp8_dense_codes(latentmoe_t h, uint8_t* x_codes, uint8_t* c_codes,
+                                  uint8_t* sh_codes, latentmoe_stream_t stream);
+
 /* Set the activation scales (host [LATENTMOE_FP8_TENSORS], finite, > 0)
  * and clear the history, e.g. from a calibration run. Synchronises the
  * device. UNSUPPORTED without LATENTMOE_FP8_EXPERTS. */
 int latentmoe_set_fp8_scales(latentmoe_t h, const float* scales);
 
-/* Scales of the loaded expert weights: host fp32 [3, E] (W_g, W_u, W_d of
- * each expert). Synchronises the device. */
+/* Scales of the loaded E4M3 weights: host fp32 [3 * E + 5]: W_g, W_u, W_d
+ * of each expert ([3, E]), then W_dn, W_up, W_gs, W_us, W_ds (1 where not
+ * quantized). Synchronises the device. */
 int latentmoe_get_fp8_weight_scales(latentmoe_t h, float* scales);
 
 /* Quantize bf16 src [groups, rows, cols] (device, cols % 16 == 0) to E4M3

@@ -28,7 +28,8 @@ ROUTER_BIAS = 2
 OUT_FP32 = 4
 SELECT_BIAS = 8
 FP8_EXPERTS = 16
-FP8_TENSORS = 2  # scaled activations: z, h
+FP8_DENSE = 32
+FP8_TENSORS = 5  # scaled activations: z, h, x, c, shared hidden
 
 STATUS_TIMEOUT = 1
 STATUS_BAD_EXPERT = 2
@@ -85,6 +86,7 @@ SIGNATURES = {
                                                ctypes.POINTER(_i64)]),
     "latentmoe_get_fp8_codes": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "latentmoe_set_fp8_scales": (ctypes.c_int, [_c_void_p, ctypes.POINTER(ctypes.c_float)]),
+    "latentmoe_get_fp8_dense_codes": (ctypes.c_int, [_c_void_p] * 5),
     "latentmoe_get_fp8_weight_scales": (ctypes.c_int, [_c_void_p,
                                                        ctypes.POINTER(ctypes.c_float)]),
     "latentmoe_quantize_e4m3": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p,
@@ -148,13 +150,14 @@ class LatentMoE:
 
     def __init__(self, d: int, l: int, E: int, k: int, F: int, Fs: int = 0,
                  max_tokens: int = 1, renorm: bool = False, router_bias: bool = False,
-                 out_fp32: bool = False, select_bias: bool = False, fp8: bool = False):
+                 out_fp32: bool = False, select_bias: bool = False, fp8: bool = False,
+                 fp8_dense: bool = False):
         lib = load()
         self.dims = latentmoe_dims(d, l, E, F, Fs, max_tokens)
         self.k = k
         self.flags = (RENORM if renorm else 0) | (ROUTER_BIAS if router_bias else 0) | \
             (OUT_FP32 if out_fp32 else 0) | (SELECT_BIAS if select_bias else 0) | \
-            (FP8_EXPERTS if fp8 else 0)
+            (FP8_EXPERTS if fp8 else 0) | (FP8_DENSE if fp8_dense else 0)
         h = _c_void_p()
         check(lib.latentmoe_create(ctypes.byref(self.dims), k, self.flags, ctypes.byref(h)),
               "latentmoe_create")
@@ -289,16 +292,35 @@ class LatentMoE:
         return zc, hc
 
     def set_fp8_scales(self, scales) -> None:
-        sc = (ctypes.c_float * FP8_TENSORS)(*scales)
+        """Scales for z, h[, x, c, shared hidden]; the ones not given are 1."""
+        vals = list(scales) + [1.0] * (FP8_TENSORS - len(scales))
+        sc = (ctypes.c_float * FP8_TENSORS)(*vals)
         check(load().latentmoe_set_fp8_scales(self.handle, sc), "latentmoe_set_fp8_scales")
 
     def fp8_weight_scales(self):
         """[3, E] list of lists: scales of W_g, W_u, W_d per expert."""
+        return self.fp8_all_weight_scales()[0]
+
+    def fp8_all_weight_scales(self):
+        """([3, E] expert scales, {w_dn, w_up, w_gs, w_us, w_ds} dense scales)."""
         E = self.dims.num_experts
-        buf = (ctypes.c_float * (3 * E))()
+        buf = (ctypes.c_float * (3 * E + 5))()
         check(load().latentmoe_get_fp8_weight_scales(self.handle, buf),
               "latentmoe_get_fp8_weight_scales")
-        return [list(buf[m * E:(m + 1) * E]) for m in range(3)]
+        dense = dict(zip(("w_dn", "w_up", "w_gs", "w_us", "w_ds"), buf[3 * E:3 * E + 5]))
+        return [list(buf[m * E:(m + 1) * E]) for m in range(3)], dense
+
+    def fp8_dense_codes(self, T: int, device, stream=None):
+        """(x codes [T, d], c codes [T, l], shared hidden codes [T, F_s] or None)."""
+        import torch
+        xc = torch.empty((T, self.dims.hidden), dtype=torch.uint8, device=device)
+        cc = torch.empty((T, self.dims.latent), dtype=torch.uint8, device=device)
+        sc = torch.empty((T, self.dims.shared_ffn), dtype=torch.uint8, device=device) \
+            if self.dims.shared_ffn else None
+        check(load().latentmoe_get_fp8_dense_codes(self.handle, xc.data_ptr(), cc.data_ptr(),
+                                                   _ptr(sc), _stream(stream)),
+              "latentmoe_get_fp8_dense_codes")
+        return xc, cc, sc
 
     def set_capacity(self, capacity: int, group_size: int = 1, max_rounds: int = 0) -> None:
         """Multi-round fixed-capacity expert schedule (capacity 0: one pass)."""

@@ -44,7 +44,10 @@ constexpr int kNumStages = 10;
 const char* const kStageNames[kNumStages] = {
     "router",      "replay_gates", "sort",           "down_proj", "expert_gate_up",
     "expert_down", "combine",      "shared_gate_up", "up_proj",   "fp8_scales"};
-constexpr int kFp8Acts = 2;  // scaled activations: 0 = z, 1 = h
+// scaled activations: 0 = z, 1 = h (expert GEMMs), 2 = x, 3 = c, 4 = the
+// shared expert's hidden (dense GEMMs)
+constexpr int kFp8Acts = LATENTMOE_FP8_TENSORS;
+constexpr int kDenseW = 5;  // E4M3 dense weights: W_dn, W_up, W_gs, W_us, W_ds
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -145,6 +148,10 @@ struct latentmoe {
   int sms = 1;
   bool loaded = false;
   bool fp8 = false;             // E4M3 expert GEMMs
+  bool fp8_dense = false;       // E4M3 latent projections and shared expert
+  float* dw_scale = nullptr;    // [kDenseW] scales of the E4M3 dense weights (in wmem)
+  uint8_t* x8 = nullptr;        // [T, d] E4M3 codes of x
+  float* y32 = nullptr;         // [T, d] fp32 partial of the E4M3 up-projection (shared expert)
   bool sm_pairs = true;         // SM-pair grouped kernels where the shapes allow
   // multi-round fixed-capacity expert schedule (capacity 0: one dropless pass)
   int64_t cap = 0;
@@ -295,6 +302,7 @@ int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok
   a.status = h->status;
   a.w_scale0 = a.w_scale1 = a.in_scale = a.out_scale = nullptr;
   a.out_amax = nullptr;
+  a.out_f32 = h->fp8_dense ? 1 : 0;
   if (h->fp8) {
     a.w_scale0 = a.w_scale1 = h->w_scale + 2 * E;
     a.in_scale = &h->f8->scale[1];
@@ -378,7 +386,9 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   const latentmoe_dims d = *dims;
   if (flags & ~static_cast<uint32_t>(LATENTMOE_RENORM | LATENTMOE_ROUTER_BIAS |
                                      LATENTMOE_OUT_FP32 | LATENTMOE_SELECT_BIAS |
-                                     LATENTMOE_FP8_EXPERTS))
+                                     LATENTMOE_FP8_EXPERTS | LATENTMOE_FP8_DENSE))
+    return LATENTMOE_ERR_INVALID_ARG;
+  if ((flags & LATENTMOE_FP8_DENSE) && !(flags & LATENTMOE_FP8_EXPERTS))
     return LATENTMOE_ERR_INVALID_ARG;
   if ((flags & LATENTMOE_ROUTER_BIAS) && (flags & LATENTMOE_SELECT_BIAS))
     return LATENTMOE_ERR_INVALID_ARG;
@@ -403,6 +413,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->k = top_k;
   h->flags = flags;
   h->fp8 = (flags & LATENTMOE_FP8_EXPERTS) != 0;
+  h->fp8_dense = (flags & LATENTMOE_FP8_DENSE) != 0;
   memset(&h->w, 0, sizeof(h->w));
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) {
@@ -427,10 +438,14 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   const size_t o_cnt = take(nb_ints * 4), o_cbase = take(nb_ints * 4);
   const size_t o_counts = take(E * 4), o_offsets = take((E + 1) * 4);
   const size_t o_lbl = take(((T + lmoe::kLblTokens - 1) / lmoe::kLblTokens) * E * 4);
-  const size_t o_zp = take(S * l * 2), o_h = take(S * F * 2), o_o = take(S * l * 2);
+  // o is kept in fp32 when it feeds the E4M3 up-projection
+  const size_t o_zp = take(S * l * 2), o_h = take(S * F * 2);
+  const size_t o_o = take(S * l * ((flags & LATENTMOE_FP8_DENSE) ? 4 : 2));
   const size_t o_c = take(T * l * 2), o_sh = take(Fs > 0 ? T * Fs * 2 : 16);
   const size_t o_status = take(16);
   const size_t o_f8 = take(sizeof(lmoe::Fp8State));
+  const size_t o_x8 = take(h->fp8_dense ? T * d.hidden : 16);
+  const size_t o_y32 = take(h->fp8_dense && Fs > 0 ? T * d.hidden * 4 : 16);
   e = cudaMalloc(&h->ws, off);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -455,6 +470,8 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->sh = reinterpret_cast<__nv_bfloat16*>(base + o_sh);
   h->status = reinterpret_cast<unsigned*>(base + o_status);
   h->f8 = reinterpret_cast<lmoe::Fp8State*>(base + o_f8);
+  h->x8 = reinterpret_cast<uint8_t*>(base + o_x8);
+  h->y32 = reinterpret_cast<float*>(base + o_y32);
   e = cudaMemset(h->status, 0, 16);
   if (e == cudaSuccess) {
     // delayed scaling starts with an empty history and unit scales
@@ -509,14 +526,17 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
     off = round_up(off + bytes, 1024);
     return o;
   };
-  const size_t o_r = take(E * dd * 2), o_b = take(bias ? E * 4 : 16), o_dn = take(l * dd * 2);
-  const size_t o_up = take(dd * l * 2);
+  // dense weights: bf16 as given, or E4M3 codes (one scale per matrix)
+  const uint64_t db = h->fp8_dense ? 1 : 2;
+  const size_t o_r = take(E * dd * 2), o_b = take(bias ? E * 4 : 16), o_dn = take(l * dd * db);
+  const size_t o_up = take(dd * l * db);
   // expert weights: packed bf16 tiles, or packed E4M3 codes plus their scales
   const uint64_t eb = h->fp8 ? 1 : 2;
   const size_t o_g = take(E * F * l * eb), o_u = take(E * F * l * eb), o_d = take(E * l * F * eb);
   const size_t o_ws = take(h->fp8 ? 3 * E * 4 : 16), o_wa = take(h->fp8 ? 3 * E * 4 : 16);
-  const size_t o_gs = take(shared ? Fs * dd * 2 : 16), o_us = take(shared ? Fs * dd * 2 : 16);
-  const size_t o_ds = take(shared ? dd * Fs * 2 : 16);
+  const size_t o_gs = take(shared ? Fs * dd * db : 16), o_us = take(shared ? Fs * dd * db : 16);
+  const size_t o_ds = take(shared ? dd * Fs * db : 16);
+  const size_t o_dws = take(kDenseW * 4), o_dwa = take(kDenseW * 4);
   // the caller's writes to its weights may still be in flight on any stream
   LMOE_CK(h, cudaDeviceSynchronize());
   h->loaded = false;
@@ -548,15 +568,39 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
     o.w_ds = base + o_ds;
   }
   h->w_scale = h->fp8 ? reinterpret_cast<float*>(base + o_ws) : nullptr;
+  h->dw_scale = reinterpret_cast<float*>(base + o_dws);
   const auto dd2d = cudaMemcpyDeviceToDevice;
   LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_r), w->w_r, E * dd * 2, dd2d));
   if (bias) LMOE_CK(h, cudaMemcpy(const_cast<float*>(o.b_r), w->b_r, E * 4, dd2d));
-  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_dn), w->w_dn, l * dd * 2, dd2d));
-  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_up), w->w_up, dd * l * 2, dd2d));
-  if (shared) {
-    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_gs), w->w_gs, Fs * dd * 2, dd2d));
-    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_us), w->w_us, Fs * dd * 2, dd2d));
-    LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_ds), w->w_ds, dd * Fs * 2, dd2d));
+  {
+    // dense weights: W_dn, W_up, W_gs, W_us, W_ds (the shared three only with F_s > 0)
+    const void* dsrc[kDenseW] = {w->w_dn, w->w_up, w->w_gs, w->w_us, w->w_ds};
+    void* ddst[kDenseW] = {const_cast<void*>(o.w_dn), const_cast<void*>(o.w_up),
+                           const_cast<void*>(o.w_gs), const_cast<void*>(o.w_us),
+                           const_cast<void*>(o.w_ds)};
+    const uint64_t drows[kDenseW] = {l, dd, Fs, Fs, dd};
+    const uint64_t dcols[kDenseW] = {dd, l, dd, dd, Fs};
+    const int nd = shared ? kDenseW : 2;
+    if (h->fp8_dense) {
+      // s = max |W| / 448 per matrix, codes row-major (the dense GEMM's layout)
+      unsigned* damax = reinterpret_cast<unsigned*>(base + o_dwa);
+      LMOE_CK(h, cudaMemset(damax, 0, kDenseW * 4));
+      for (int m = 0; m < nd; ++m)
+        LMOE_CK(h, lmoe::launch_absmax_groups(static_cast<const __nv_bfloat16*>(dsrc[m]), 1,
+                                              static_cast<long long>(drows[m] * dcols[m]),
+                                              damax + m, h->sms, 0));
+      LMOE_CK(h, lmoe::launch_scales_from_amax(damax, kDenseW, h->dw_scale, 0));
+      for (int m = 0; m < nd; ++m)
+        LMOE_CK(h, lmoe::launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(dsrc[m]),
+                                              static_cast<uint8_t*>(ddst[m]),
+                                              static_cast<long long>(drows[m]),
+                                              static_cast<long long>(dcols[m]),
+                                              static_cast<long long>(drows[m]), h->dw_scale + m,
+                                              false, h->sms, 0));
+    } else {
+      for (int m = 0; m < nd; ++m)
+        LMOE_CK(h, cudaMemcpy(ddst[m], dsrc[m], drows[m] * dcols[m] * 2, dd2d));
+    }
   }
   typedef const __nv_bfloat16* cbf;
   const void* srcs[3] = {w->w_g, w->w_u, w->w_d};
@@ -588,16 +632,28 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   bool ok = true;
   ok &= make_map(&h->m_router.b, o.w_r, E, dd, dd, 256);
   ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);
-  ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
+  if (h->fp8_dense)
+    ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 256);
+  else
+    ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
   // tiles of 128 rows x 128 bytes
   ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l * eb / 128), h->fp8);
   ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l * eb / 128), h->fp8);
   ok &= make_tile_map(&h->m_wd, o.w_d, E * l / 128 * (F * eb / 128), h->fp8);
-  ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 256);
-  if (shared) {
-    ok &= make_map(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
-    ok &= make_map(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
-    ok &= make_map(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
+  if (h->fp8_dense) {
+    ok &= make_map_u8(&h->m_up.b, o.w_up, dd, l, l, 256);
+    if (shared) {
+      ok &= make_map_u8(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
+      ok &= make_map_u8(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
+      ok &= make_map_u8(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
+    }
+  } else {
+    ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 256);
+    if (shared) {
+      ok &= make_map(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
+      ok &= make_map(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
+      ok &= make_map(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
+    }
   }
   if (!ok) return LATENTMOE_ERR_CUDA;
   // unused map slots still travel as kernel parameters: give them a valid copy
@@ -634,8 +690,16 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   ok &= make_map(&mx32, x, T, dd, dd, 128, lmoe::kRBK);
   ok &= make_token_map(&mzp, h->zp, S, l, h->fp8);
   ok &= make_token_map(&mh, h->hb, S, F, h->fp8);
-  ok &= make_map(&mc, h->cb, T, l, l, 128);
-  if (Fs > 0) ok &= make_map(&msh, h->sh, T, Fs, Fs, 128);
+  CUtensorMap mx8;
+  if (h->fp8_dense) {
+    // E4M3 codes of x, c and the shared hidden, 128-row boxes
+    ok &= make_map_u8(&mx8, h->x8, T, dd, dd, 128);
+    ok &= make_map_u8(&mc, h->cb, T, l, l, 128);
+    if (Fs > 0) ok &= make_map_u8(&msh, h->sh, T, Fs, Fs, 128);
+  } else {
+    ok &= make_map(&mc, h->cb, T, l, l, 128);
+    if (Fs > 0) ok &= make_map(&msh, h->sh, T, Fs, Fs, 128);
+  }
   if (!ok) return LATENTMOE_ERR_CUDA;
 
   const int slot_base = h->prof_slots > 0
@@ -684,15 +748,22 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     if (r != LATENTMOE_OK) return r;
   }
   record(h, slot_base, 3, s);
-  // 3: latent down-projection scattered to the expert-sorted slots
+  // 3: latent down-projection scattered to the expert-sorted slots (with
+  // E4M3 dense GEMMs, x is quantized first)
+  if (h->fp8_dense) {
+    LMOE_CK(h, lmoe::launch_quantize_act(static_cast<const __nv_bfloat16*>(x), h->x8,
+                                         static_cast<long long>(T) * dd, &h->f8->scale[2],
+                                         &h->f8->amax[2], h->sms, s));
+    h->launches += 1;
+  }
   {
     GemmMaps m = h->m_down;
-    m.a = mx;
+    m.a = h->fp8_dense ? mx8 : mx;
     GemmArgs a = base_args(h);
     a.M = Ti;
     a.N = l;
     a.n_tiles = ceil_div(l, lmoe::kBN);
-    a.kb1 = dd / lmoe::kBK;
+    a.kb1 = dd / (h->fp8_dense ? lmoe::kBK8 : lmoe::kBK);
     a.out = h->zp;
     a.ldo = l;
     a.pos = h->pos;
@@ -700,7 +771,10 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     if (h->fp8) {
       a.out_scale = &h->f8->scale[0];
       a.out_amax = &h->f8->amax[0];
-      LMOE_CK(h, lmoe::launch_gemm_scatter_f8(m, a, dense_grid(h, Ti, a.n_tiles), s));
+      a.a_scale = &h->f8->scale[2];
+      a.b_scale = &h->dw_scale[0];
+      LMOE_CK(h, lmoe::launch_gemm_scatter_f8(m, a, dense_grid(h, Ti, a.n_tiles), s,
+                                              h->fp8_dense));
     } else {
       LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s));
     }
@@ -728,27 +802,85 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     if (r != LATENTMOE_OK) return r;
   }
   record(h, slot_base, 6, s);
-  // 6: combine
-  LMOE_CK(h, lmoe::launch_combine(h->ob, h->gates, h->pos, Ti, k, l, h->cb, s));
+  // 6: combine (E4M3 dense GEMMs: c written as codes)
+  if (h->fp8_dense)
+    LMOE_CK(h, lmoe::launch_combine_f8(reinterpret_cast<const float*>(h->ob), h->gates, h->pos,
+                                       Ti, k, l,
+                                       reinterpret_cast<uint8_t*>(h->cb), &h->f8->scale[3],
+                                       &h->f8->amax[3], s));
+  else
+    LMOE_CK(h, lmoe::launch_combine(h->ob, h->gates, h->pos, Ti, k, l, h->cb, s));
   h->launches += 1;
   record(h, slot_base, 7, s);
   // 7: shared expert gate+up on the full width
   if (Fs > 0) {
     GemmMaps m = h->m_shared;
-    m.a = mx;
+    m.a = h->fp8_dense ? mx8 : mx;
     GemmArgs a = base_args(h);
     a.M = Ti;
     a.N = Fs;
     a.n_tiles = Fs / (lmoe::kBN / 2);
-    a.kb1 = dd / lmoe::kBK;
+    a.kb1 = dd / (h->fp8_dense ? lmoe::kBK8 : lmoe::kBK);
     a.out = h->sh;
     a.ldo = Fs;
-    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, dense_grid(h, Ti, a.n_tiles), s));
+    if (h->fp8_dense) {
+      a.a_scale = &h->f8->scale[2];
+      a.b_scale = &h->dw_scale[2];
+      a.b_scale2 = &h->dw_scale[3];
+      a.out_scale = &h->f8->scale[4];
+      a.out_amax = &h->f8->amax[4];
+    }
+    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, dense_grid(h, Ti, a.n_tiles), s, h->fp8_dense));
     h->launches += 1;
   }
   record(h, slot_base, 8, s);
-  // 8: up-projection (+ shared expert's down-projection, K-concatenated)
-  {
+  // 8: up-projection (+ shared expert's down-projection, K-concatenated; with
+  // E4M3 dense GEMMs the two products have their own scales: the
+  // up-projection leaves an fp32 partial that the shared down GEMM adds)
+  if (h->fp8_dense) {
+    GemmArgs a = base_args(h);
+    a.M = Ti;
+    a.N = dd;
+    a.n_tiles = ceil_div(dd, lmoe::kBN);
+    a.a_scale = &h->f8->scale[3];
+    a.b_scale = &h->dw_scale[1];
+    a.kb1 = l / lmoe::kBK8;
+    const int grid = dense_grid(h, Ti, a.n_tiles);
+    GemmMaps m = h->m_up;
+    m.a = mc;
+    m.a2 = mc;
+    m.b2 = h->m_up.b;
+    if (Fs > 0) {
+      a.out = h->y32;
+      a.ldo = dd;
+      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true));
+      h->launches += 1;
+      GemmMaps m2 = h->m_up;
+      m2.a = msh;
+      m2.b = h->m_up.b2;
+      m2.a2 = msh;
+      GemmArgs b = a;
+      b.a_scale = &h->f8->scale[4];
+      b.b_scale = &h->dw_scale[4];
+      b.kb1 = Fs / lmoe::kBK8;
+      b.addend = h->y32;
+      b.ld_add = dd;
+      b.out = out;
+      b.ldo = dd;
+      if (out32)
+        LMOE_CK(h, lmoe::launch_gemm_f32(m2, b, grid, false, s, true));
+      else
+        LMOE_CK(h, lmoe::launch_gemm_bf16(m2, b, grid, false, s, true));
+    } else {
+      a.out = out;
+      a.ldo = dd;
+      if (out32)
+        LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true));
+      else
+        LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, false, s, true));
+    }
+    h->launches += 1;
+  } else {
     GemmMaps m = h->m_up;
     m.a = mc;
     if (Fs > 0) m.a2 = msh; else m.a2 = mc;
@@ -1075,6 +1207,31 @@ int latentmoe_get_fp8_weight_scales(latentmoe_t h, float* scales) {
   LMOE_CK(h, cudaSetDevice(h->device));
   LMOE_CK(h, cudaDeviceSynchronize());
   LMOE_CK(h, cudaMemcpy(scales, h->w_scale, 3 * h->dims.num_experts * 4, cudaMemcpyDeviceToHost));
+  float* dense = scales + 3 * h->dims.num_experts;
+  if (h->fp8_dense) {
+    LMOE_CK(h, cudaMemcpy(dense, h->dw_scale, kDenseW * 4, cudaMemcpyDeviceToHost));
+  } else {
+    for (int i = 0; i < kDenseW; ++i) dense[i] = 1.0f;
+  }
+  return LATENTMOE_OK;
+}
+
+int latentmoe_get_fp8_dense_codes(latentmoe_t h, uint8_t* x_codes, uint8_t* c_codes,
+                                  uint8_t* sh_codes, latentmoe_stream_t st) {
+  if (h == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->fp8_dense) return LATENTMOE_ERR_UNSUPPORTED;
+  if (h->last_T < 1 || (sh_codes != nullptr && h->dims.shared_ffn == 0))
+    return LATENTMOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const size_t T = static_cast<size_t>(h->last_T);
+  if (x_codes)
+    LMOE_CK(h, cudaMemcpyAsync(x_codes, h->x8, T * h->dims.hidden, cudaMemcpyDeviceToDevice, s));
+  if (c_codes)
+    LMOE_CK(h, cudaMemcpyAsync(c_codes, h->cb, T * h->dims.latent, cudaMemcpyDeviceToDevice, s));
+  if (sh_codes)
+    LMOE_CK(h, cudaMemcpyAsync(sh_codes, h->sh, T * h->dims.shared_ffn, cudaMemcpyDeviceToDevice,
+                               s));
   return LATENTMOE_OK;
 }
 

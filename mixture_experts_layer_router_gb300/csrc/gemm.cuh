@@ -26,6 +26,15 @@
 //   kEpiScatter  token row t is written to rows pos[t*k + j], j < k, of C
 //   kEpiScatterF8  the same with C as E4M3 codes of acc / out_scale, and the
 //                running max |acc| of the valid rows recorded in out_amax
+//   kEpiSwigluF8 the SwiGLU epilogue with C as E4M3 codes of h / out_scale
+//                (max |h| of the valid rows recorded in out_amax)
+//
+// E4M3 operands (F8 = true): A and B are E4M3 codes, a k-block is 128 codes
+// (still one 128-byte swizzle row), the MMA is kind::f8f6f4, and the
+// accumulator is multiplied by a_scale * b_scale (SwiGLU: b_scale for the
+// gate columns, b_scale2 for the up columns) before the epilogue. An fp32
+// `addend` [rows, ld_add] is added to the scaled accumulator of kEpiBf16 /
+// kEpiF32 before rounding (the shared expert's partial sum).
 //
 // Ragged edges: rows past a segment or past M are computed on whatever TMA
 // brought in (zeros past the tensor) and never stored; columns past N are not
@@ -37,11 +46,19 @@
 
 namespace lmoe {
 
-enum EpiMode : int { kEpiBf16 = 0, kEpiF32 = 1, kEpiSwiglu = 2, kEpiScatter = 3, kEpiScatterF8 = 4 };
+enum EpiMode : int {
+  kEpiBf16 = 0,
+  kEpiF32 = 1,
+  kEpiSwiglu = 2,
+  kEpiScatter = 3,
+  kEpiScatterF8 = 4,
+  kEpiSwigluF8 = 5
+};
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kBK8 = 128;  // 128 E4M3 codes = one swizzle row
 constexpr int kStages = 4;
 constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kBTileBytes = kBN * kBK * 2;
@@ -76,8 +93,13 @@ struct GemmArgs {
   int topk;
   unsigned* status;        // device status word
   int hints;               // bit 0: A tiles evict_last in L2; bit 1: B tiles evict_first
-  const float* out_scale;  // kEpiScatterF8: [1] scale the output is quantized with
-  unsigned* out_amax;      // kEpiScatterF8: [1] running max |acc| (float bits)
+  const float* out_scale;  // kEpiScatterF8 / kEpiSwigluF8: [1] scale the output is quantized with
+  unsigned* out_amax;      // kEpiScatterF8 / kEpiSwigluF8: [1] running max (float bits)
+  const float* a_scale;    // E4M3 operands: [1] scale of A
+  const float* b_scale;    // E4M3 operands: [1] scale of B (SwiGLU: gate rows)
+  const float* b_scale2;   // E4M3 SwiGLU: [1] scale of the up rows
+  const float* addend;     // kEpiBf16 / kEpiF32: fp32 [rows, ld_add] added before rounding, or null
+  long long ld_add;
 };
 
 struct TileCoord {
@@ -170,7 +192,8 @@ __device__ __forceinline__ void store_chunk_bf16_staged(const GemmArgs& a,
   __syncwarp();
 }
 
-// E4M3 output of one 32-column chunk, scattered like kEpiScatter: each lane
+// E4M3 output of one 32-column chunk, scattered like kEpiScatter (or to the
+// lane's own row when a.pos is null): each lane
 // quantizes its row to 32 bytes, the warp stages them (16-byte pieces
 // XOR-swizzled by row / 4, conflict-free both ways) and writes 16 rows per
 // instruction, 2 lanes per row.
@@ -202,11 +225,16 @@ __device__ __forceinline__ void store_chunk_f8_scatter(const GemmArgs& a, const 
         *reinterpret_cast<const uint4*>(stage + rr * 32 + ((piece ^ ((rr >> 2) & 1)) * 16));
     if (rr < rows_valid) {
       const long long row = warp_row0 + rr;
-      for (int j = 0; j < a.topk; ++j) {
-        const int dst_row = a.pos[row * a.topk + j];
-        if (dst_row < 0) continue;
-        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
-                                  static_cast<long long>(dst_row) * a.ldo + col + piece * 16) = w;
+      if (a.pos == nullptr) {
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + row * a.ldo + col + piece * 16) =
+            w;
+      } else {
+        for (int j = 0; j < a.topk; ++j) {
+          const int dst_row = a.pos[row * a.topk + j];
+          if (dst_row < 0) continue;
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                    static_cast<long long>(dst_row) * a.ldo + col + piece * 16) = w;
+        }
       }
     }
   }
@@ -266,7 +294,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&
   }
 }
 
-template <int MODE, bool DUAL>
+template <int MODE, bool DUAL, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBu,
@@ -289,7 +317,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int kBRowsPerTile = (MODE == kEpiSwiglu) ? kBN / 2 : kBN;
+  constexpr bool kSwiglu = MODE == kEpiSwiglu || MODE == kEpiSwigluF8;
+  constexpr int kBRowsPerTile = kSwiglu ? kBN / 2 : kBN;
+  constexpr int kKB = F8 ? kBK8 : kBK;  // elements per k-block
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -308,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE == kEpiSwiglu) tma_prefetch_desc(&tmBu);
+    if (kSwiglu) tma_prefetch_desc(&tmBu);
     if (DUAL) {
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
@@ -372,16 +402,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = sa + kATileBytes;
           mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
           if (!DUAL || kb < a.kb1) {
-            const int kc = kb * kBK;
+            const int kc = kb * kKB;
             tma_load_2d(&tmA, &full_bar[stage], sa, kc, c.row0, pol);
-            if (MODE == kEpiSwiglu) {
+            if (kSwiglu) {
               tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
               tma_load_2d(&tmBu, &full_bar[stage], sb + kBTileBytes / 2, kc, c.brow, pol_b);
             } else {
               tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
             }
           } else {
-            const int kc = (kb - a.kb1) * kBK;
+            const int kc = (kb - a.kb1) * kKB;
             tma_load_2d(&tmA2, &full_bar[stage], sa, kc, c.row0, pol);
             tma_load_2d(&tmB2, &full_bar[stage], sb, kc, c.brow, pol_b);
           }
@@ -400,7 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = instr_desc_bf16(kBM, kBN);
+      constexpr uint32_t idesc = F8 ? instr_desc_e4m3(kBM, kBN) : instr_desc_bf16(kBM, kBN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -420,9 +450,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t da = smem_desc_sw128(sa);
           const uint64_t db = smem_desc_sw128(sa + kATileBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
+          for (int k = 0; k < 4; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in addr>>4
-            tc_mma(d_tmem, da + 2ull * k, db + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (F8)
+              tc_mma_f8(d_tmem, da + 2ull * k, db + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              tc_mma(d_tmem, da + 2ull * k, db + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == kStages) {
@@ -448,7 +481,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* stage_w = stage_smem + (warp - 2) * kStageWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const float out_inv = MODE == kEpiScatterF8 ? inv_scale(*a.out_scale) : 1.0f;
+    const float out_inv =
+        (MODE == kEpiScatterF8 || MODE == kEpiSwigluF8) ? inv_scale(*a.out_scale) : 1.0f;
+    // E4M3 operands: accumulator scale (SwiGLU: gate columns; up columns below)
+    const float acc_s = F8 ? (*a.a_scale) * (*a.b_scale) : 1.0f;
+    const float acc_s2 = (F8 && kSwiglu) ? (*a.a_scale) * (*a.b_scale2) : 1.0f;
     float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const TileCoord c = decode_tile(t, a, seg_s, mt_s, kBRowsPerTile);
@@ -460,7 +497,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const long long row = static_cast<long long>(c.row0) + r;
       const long long warp_row0 = static_cast<long long>(c.row0) + quarter * 32;
       const int warp_rows = c.rows - quarter * 32;
-      if constexpr (MODE == kEpiSwiglu) {
+      if constexpr (kSwiglu) {
 #pragma unroll 1
         for (int ch = 0; ch < kBN / 64; ++ch) {
           uint32_t g[32], u[32];
@@ -471,8 +508,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (col < a.N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              g[i] = __float_as_uint(silu(__uint_as_float(g[i])) * __uint_as_float(u[i]));
-            store_chunk_bf16_staged<kEpiBf16>(a, g, stage_w, warp_row0, warp_rows, col);
+              g[i] = __float_as_uint(silu(__uint_as_float(g[i]) * acc_s) *
+                                     (__uint_as_float(u[i]) * acc_s2));
+            if constexpr (MODE == kEpiSwigluF8) {
+              if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(g[i])));
+              }
+              store_chunk_f8_scatter(a, g, out_inv, stage_w, warp_row0, warp_rows, col);
+            } else {
+              store_chunk_bf16_staged<kEpiBf16>(a, g, stage_w, warp_row0, warp_rows, col);
+            }
           }
         }
       } else {
@@ -482,6 +528,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_32cols(tbase + ch * 32, v);
           tmem_ld_wait();
           const int col = c.n * kBN + ch * 32;
+          if constexpr (F8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * acc_s);
+          }
+          if constexpr (MODE == kEpiBf16 || MODE == kEpiF32) {
+            if (a.addend != nullptr && row_ok && col < a.N) {
+              // the lane's own row: 32 consecutive fp32 of the partial sum
+              const float4* src = reinterpret_cast<const float4*>(a.addend + row * a.ld_add + col);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 f = src[q];
+                v[4 * q + 0] = __float_as_uint(__uint_as_float(v[4 * q + 0]) + f.x);
+                v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + f.y);
+                v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + f.z);
+                v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + f.w);
+              }
+            }
+          }
           if constexpr (MODE == kEpiF32) {
             if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
           } else if constexpr (MODE == kEpiScatterF8) {
@@ -504,7 +568,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if constexpr (MODE == kEpiScatterF8) {
+    if constexpr (MODE == kEpiScatterF8 || MODE == kEpiSwigluF8) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(a.out_amax, amax);
     }

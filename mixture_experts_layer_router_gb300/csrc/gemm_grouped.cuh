@@ -81,8 +81,10 @@ struct GroupedArgs {
   int kb;                  // k-blocks (K / 64)
   int w_group_rows;        // weight rows per group in the weight maps
   int n_out;               // output features (columns of out)
-  void* out;               // bf16 [rows, n_out] (E4M3 SwiGLU: codes), rows in slot order
+  void* out;               // bf16 [rows, n_out] (E4M3 SwiGLU: codes; plain with out_f32:
+                           // fp32), rows in slot order
   long long ldo;
+  int out_f32;             // plain: fp32 output
   unsigned* status;
   // E4M3 variant only
   const float* w_scale0;   // [G] scale of the weights of accumulator 0, per group
@@ -237,6 +239,18 @@ __device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_
 // 32 tokens (token 4j+b in byte b of q[j]). Each token row segment is 32
 // bytes; pieces are XOR-swizzled by (row / 4) so that both the byte writes
 // and the 16-byte reads are free of bank conflicts.
+// fp32 output of one 32-token chunk: for each token the warp's 32 lanes hold
+// 32 consecutive features, one 128-byte store per token row.
+__device__ __forceinline__ void gstore_chunk_f32(const GroupedArgs& a, const uint32_t (&v)[32],
+                                                 float scale, long long tok_row0, int tok_valid,
+                                                 int feat0) {
+  const int lane = threadIdx.x & 31;
+  float* out = static_cast<float*>(a.out) + feat0 + lane;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < tok_valid) out[(tok_row0 + j) * a.ldo] = __uint_as_float(v[j]) * scale;
+}
+
 __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint32_t (&q)[8],
                                                 uint8_t* stage, long long tok_row0,
                                                 int tok_valid, int feat0) {
@@ -501,12 +515,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
             tmem_ld_wait();
             const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
+            const int feat0 = c.f * 256 + acc * 128 + quarter * 32;
+            if (a.out_f32) {
+              if (feat0 < a.n_out) gstore_chunk_f32(a, v, so, tok_row0, tok_valid, feat0);
+              continue;
+            }
             uint32_t o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
                                  __uint_as_float(v[2 * j + 1]) * so);
-            const int feat0 = c.f * 256 + acc * 128 + quarter * 32;
             if (feat0 < a.n_out) gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
           }
         }

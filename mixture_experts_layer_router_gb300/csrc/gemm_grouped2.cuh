@@ -319,12 +319,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             uint32_t v[32];
             tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
             tmem_ld_wait();
+            const int feat0 = c.p * 512 + acc * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+            if (a.out_f32) {
+              gstore_chunk_f32(a, v, so, tok_row0, tok_valid, feat0);
+              continue;
+            }
             uint32_t o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
                                  __uint_as_float(v[2 * j + 1]) * so);
-            const int feat0 = c.p * 512 + acc * 256 + static_cast<int>(rank) * 128 + quarter * 32;
             gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
           }
         }

@@ -6,19 +6,19 @@
 
 namespace lmoe {
 
-template <int MODE, bool DUAL>
+template <int MODE, bool DUAL, bool F8 = false>
 static cudaError_t launch_gemm_impl(const GemmMaps& m, const GemmArgs& a, int grid,
                                     cudaStream_t s) {
   static bool smem_set = false;
   if (!smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, DUAL>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, DUAL, F8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kGemmSmemBytes);
     if (e != cudaSuccess) return e;
     smem_set = true;
   }
-  gemm_tc_kernel<MODE, DUAL><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(m.a, m.b, m.bu, m.a2,
-                                                                        m.b2, a);
+  gemm_tc_kernel<MODE, DUAL, F8><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(m.a, m.b, m.bu, m.a2,
+                                                                            m.b2, a);
   return cudaGetLastError();
 }
 

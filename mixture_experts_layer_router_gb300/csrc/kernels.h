@@ -15,16 +15,20 @@ struct GemmMaps {
   CUtensorMap a, b, bu, a2, b2;
 };
 
-// One launch of gemm_tc_kernel<MODE, DUAL>; `grid` persistent CTAs.
+// One launch of gemm_tc_kernel<MODE, DUAL, F8>; `grid` persistent CTAs.
+// f8: E4M3 operands (a_scale, b_scale set; not with dual).
 cudaError_t launch_gemm_bf16(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
-                             cudaStream_t s);
+                             cudaStream_t s, bool f8 = false);
 cudaError_t launch_gemm_f32(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
-                            cudaStream_t s);
-cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+                            cudaStream_t s, bool f8 = false);
+// SwiGLU epilogue; with f8 the output is E4M3 codes (out_scale, out_amax,
+// b_scale2 set).
+cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s,
+                               bool f8 = false);
 cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
 // kEpiScatterF8: the scatter with E4M3 output (out_scale, out_amax set).
 cudaError_t launch_gemm_scatter_f8(const GemmMaps& m, const GemmArgs& a, int grid,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool f8 = false);
 
 // One launch of gemm_grouped_kernel<mode, f8> (kGrpSwiglu or kGrpPlain;
 // bf16 or E4M3 operands): tok = token rows (64-row boxes), w0/w1 = packed
@@ -66,7 +70,7 @@ cudaError_t launch_quantize_e4m3(const __nv_bfloat16* src, uint8_t* dst, long lo
 // Delayed scaling of n activation tensors (n <= kFp8Tensors): enter this
 // forward's maxima into the 1024-step history, form the next scales, clear
 // the maxima. One launch of one block.
-constexpr int kFp8Tensors = 4;
+constexpr int kFp8Tensors = 8;
 constexpr int kFp8History = 1024;
 struct Fp8State {
   float scale[kFp8Tensors];      // scales the next forward quantizes with
@@ -121,5 +125,13 @@ cudaError_t launch_round_schedule(const int* counts, const int* offsets, int E, 
 // c[t] = sum_j gates[t,j] * o[pos[t,j]] in fp32, j order; bf16 out.
 cudaError_t launch_combine(const __nv_bfloat16* o, const float* gates, const int* pos, int T,
                            int k, int l, __nv_bfloat16* c, cudaStream_t s);
+// The same from fp32 o, with c written as E4M3 codes with *scale and max |c|
+// into *amax.
+cudaError_t launch_combine_f8(const float* o, const float* gates, const int* pos, int T, int k,
+                              int l, uint8_t* c, const float* scale, unsigned* amax,
+                              cudaStream_t s);
+// E4M3 codes of bf16 src [n] (n % 16 == 0) with *scale; max |src| into *amax.
+cudaError_t launch_quantize_act(const __nv_bfloat16* src, uint8_t* dst, long long n,
+                                const float* scale, unsigned* amax, int sms, cudaStream_t s);
 
 }  // namespace lmoe

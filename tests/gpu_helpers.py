@@ -50,11 +50,12 @@ def oracle_weights(w, stacked: bool = True) -> ref.OracleWeights:
 
 
 def make_layer(cfg: synth.LayerConfig, w, max_tokens=None, renorm=False, out_fp32=False,
-               fp8=False):
+               fp8=False, fp8_dense=False):
     lib()
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs,
                            max_tokens=max_tokens or cfg.T, renorm=renorm,
-                           router_bias=w["b_r"] is not None, out_fp32=out_fp32, fp8=fp8)
+                           router_bias=w["b_r"] is not None, out_fp32=out_fp32, fp8=fp8,
+                           fp8_dense=fp8_dense)
     layer.load_weights(w)
     return layer
 

@@ -181,7 +181,7 @@ def _check_fp8_layer(cfg, w, x, layer, renorm=False):
     T = x.shape[0]
     layer.forward(x)
     st = layer.fp8_state()
-    s_z, s_h = st["scales"]
+    s_z, s_h = st["scales"][:2]
     y = layer.forward(x)
     r = layer.get_routing(T, "cuda")
     zc, hc = layer.fp8_codes(T, "cuda")
@@ -210,7 +210,7 @@ def _check_fp8_layer(cfg, w, x, layer, renorm=False):
     assert rel <= gh.Y_REL_FRO and rel < 0.3 * rel_fp8, (rel, rel_fp8)
     st2 = layer.fp8_state()
     assert st2["steps"] == 2
-    az, ah = st2["last_amax"]
+    az, ah = st2["last_amax"][:2]
     assert abs(az - ora["z_amax"]) <= 1e-3 * ora["z_amax"]
     assert abs(ah - ora["h_amax"]) <= 1e-2 * ora["h_amax"]
     return st, st2
@@ -259,7 +259,7 @@ def test_set_scales_errors_and_launch_count():
     cfg, w, x, layer = _layer_case("tiny", seed=2)
     layer.set_fp8_scales([0.01, 0.02])
     st = layer.fp8_state()
-    assert st["scales"] == [np.float32(0.01), np.float32(0.02)] and st["steps"] == 0
+    assert st["scales"][:2] == [np.float32(0.01), np.float32(0.02)] and st["steps"] == 0
     for bad in ([0.0, 1.0], [-1.0, 1.0], [float("inf"), 1.0], [1.0, float("nan")]):
         with pytest.raises(capi.LatentMoEError):
             layer.set_fp8_scales(bad)

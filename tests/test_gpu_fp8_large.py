@@ -28,7 +28,7 @@ def test_large_shape_e4m3_sampled(name, n_y):
     x = synth.make_x(cfg, 0, "cuda")
     layer = gh.make_layer(cfg, w, fp8=True)
     layer.forward(x)
-    s_z, s_h = layer.fp8_state()["scales"]
+    s_z, s_h = layer.fp8_state()["scales"][:2]
     y = layer.forward(x)
     r = layer.get_routing(cfg.T, "cuda")
     zc, hc = layer.fp8_codes(cfg.T, "cuda")
