@@ -33,6 +33,8 @@ if ROOT not in sys.path:
 METRIC = "LatentMoE bf16 fwd tokens/s at MAI-Base-1 shape; % of tensor-core roofline"
 METRIC_FP8 = ("LatentMoE fwd tokens/s at MAI-Base-1 shape with FP8 E4M3 expert GEMMs; "
               "% of tensor-core roofline")
+METRIC_FP8_DENSE = ("LatentMoE fwd tokens/s at MAI-Base-1 shape with FP8 E4M3 GEMMs (router "
+                    "fp32); % of tensor-core roofline")
 # dense E4M3 tensor rate over dense bf16 (nominal 4.5 vs 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -52,11 +54,13 @@ def expert_flops_per_token(c) -> int:
     return 6 * c.k * c.l * c.F
 
 
-def layer_bytes(c, touched_experts: int, eb: int = 2) -> int:
+def layer_bytes(c, touched_experts: int, eb: int = 2, db: int = 2) -> int:
     """Algorithmic bytes: weights read once (experts that got tokens only,
-    eb bytes per expert weight), x read once, y written once; intermediates
-    excluded as avoidable."""
-    w = touched_experts * 3 * c.l * c.F * eb + (c.E * c.d + 2 * c.l * c.d + 3 * c.d * c.Fs) * 2
+    eb bytes per expert weight, db per latent-projection and shared-expert
+    weight; the router's weights in bf16), x read once, y written once;
+    intermediates excluded as avoidable."""
+    w = touched_experts * 3 * c.l * c.F * eb + c.E * c.d * 2 + \
+        (2 * c.l * c.d + 3 * c.d * c.Fs) * db
     return w + c.T * c.d * 2 * 2
 
 
@@ -171,7 +175,8 @@ class ClockSampler:
 
 def oracle_tokens_per_s(cfg, x_rows, logits_rows, fetch, repeats=1, fp8_scales=None):
     """Time the float64 oracle on given token rows; returns (tokens/s, s).
-    With fp8_scales (s_z, s_h) the oracle's E4M3 expert layer is timed."""
+    With fp8_scales (s_z, s_h) the oracle's E4M3 expert layer is timed; with
+    (s_z, s_h, s_x, s_c, s_sh) the all-E4M3 layer."""
     from oracle import latentmoe_ref as ref
     from oracle import fp8 as ofp8
     import numpy as np
@@ -184,8 +189,10 @@ def oracle_tokens_per_s(cfg, x_rows, logits_rows, fetch, repeats=1, fp8_scales=N
         if fp8_scales is None:
             ref.forward(xr, W, cfg.k, logits=logits_rows)
         else:
+            dense = None if len(fp8_scales) == 2 else \
+                {"s_x": fp8_scales[2], "s_c": fp8_scales[3], "s_sh": fp8_scales[4]}
             ofp8.forward_fp8(xr, W, cfg.k, s_z=fp8_scales[0], s_h=fp8_scales[1],
-                             logits=logits_rows)
+                             logits=logits_rows, dense=dense)
     dt = time.perf_counter() - t0
     return x_rows.shape[0] * repeats / dt, dt
 
@@ -295,9 +302,9 @@ def run_ours(args, cfg, rank, world, dist):
     capi.load()
     w = synth.make_weights(cfg, 0, "cuda")
     x = synth.make_x(cfg, 0, "cuda")
-    f8 = args.fp8
+    f8 = args.fp8 or args.fp8_dense
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
-                           router_bias=w["b_r"] is not None, fp8=f8)
+                           router_bias=w["b_r"] is not None, fp8=f8, fp8_dense=args.fp8_dense)
     layer.load_weights(w)
     if args.no_sm_pairs:
         layer.set_sm_pairs(False)
@@ -383,7 +390,8 @@ def run_ours(args, cfg, rank, world, dist):
         need = sorted(set(r["idx"][tsel].cpu().numpy().ravel().tolist()))
         fetch = host_weights(cfg, w, need)
         xs = x[tsel].float().cpu().numpy().astype(np.float64)
-        scales = layer.fp8_state()["scales"] if f8 else None
+        scales = (layer.fp8_state()["scales"] if args.fp8_dense else
+                  layer.fp8_state()["scales"][:2]) if f8 else None
         tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch, fp8_scales=scales)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
                "sample": f"{n} seeded tokens of the {cfg.name} workload ({dt:.1f} s), float64 "
@@ -396,10 +404,14 @@ def run_ours(args, cfg, rank, world, dist):
     value = world * cfg.T * args.steps / (ms_total / 1e3)
     flops_tok = layer_flops_per_token(cfg)
     eb = 1 if f8 else 2
-    lbytes = layer_bytes(cfg, touched, eb)
+    lbytes = layer_bytes(cfg, touched, eb, 1 if args.fp8_dense else 2)
     bf16_peak = peaks["bf16_tflops_sustained"] * 1e12
-    # expert FLOPs at the E4M3 rate when they run in E4M3
+    # FLOPs at the E4M3 rate where they run in E4M3 (experts; with --fp8-dense
+    # everything but the router)
+    router_flops = cfg.T * 2 * cfg.d * cfg.E
     x_flops = cfg.T * expert_flops_per_token(cfg)
+    if args.fp8_dense:
+        x_flops = cfg.T * flops_tok - router_flops
     o_flops = cfg.T * flops_tok - x_flops
     tc_ms = (o_flops / bf16_peak + x_flops / (bf16_peak * (FP8_OVER_BF16 if f8 else 1.0))) * 1e3
     hbm_ms = lbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
@@ -424,10 +436,12 @@ def run_ours(args, cfg, rank, world, dist):
                  "peak_source": f"{peak_src} ({peak_kind})"})
 
     line = {
-        "metric": METRIC_FP8 if f8 else METRIC, "value": value, "unit": "tokens/s",
+        "metric": METRIC_FP8_DENSE if args.fp8_dense else (METRIC_FP8 if f8 else METRIC),
+        "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 experts, bf16 elsewhere" if f8 else "bf16",
+        "dtype": ("e4m3 GEMMs, fp32 router" if args.fp8_dense else
+                  "e4m3 experts, bf16 elsewhere") if f8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
         "config": {**workload_config(cfg),
                    "expert_gemm": "single-SM" if args.no_sm_pairs else "SM pairs where shapes allow",
@@ -448,7 +462,8 @@ def run_ours(args, cfg, rank, world, dist):
         "device_status": status,
     }
     if f8:
-        line["fp8_scales"] = {"z": fp8_state["scales"][0], "h": fp8_state["scales"][1],
+        names = ("z", "h", "x", "c", "shared_hidden") if args.fp8_dense else ("z", "h")
+        line["fp8_scales"] = {**dict(zip(names, fp8_state["scales"])),
                               "history_steps": fp8_state["steps"]}
     return line
 
@@ -468,6 +483,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 E4M3 expert GEMMs with delayed scaling")
+    ap.add_argument("--fp8-dense", action="store_true",
+                    help="with --fp8: the latent projections and the shared expert in E4M3 too")
     ap.add_argument("--no-sm-pairs", action="store_true",
                     help="expert GEMMs on single SMs instead of SM pairs (comparison runs)")
     ap.add_argument("--capacity", type=int, default=0,
@@ -481,7 +498,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.cpu_tokens is None:
-        args.cpu_tokens = 2 if args.fp8 else 48
+        args.cpu_tokens = 2 if (args.fp8 or args.fp8_dense) else 48
 
     from mixture_experts_layer_router_gb300 import synth
     cfg = synth.CONFIGS[args.config]
