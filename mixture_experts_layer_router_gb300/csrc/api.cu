@@ -127,15 +127,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// SM count of the current device (looked up once per device).
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
+  static int n_of[lmoe::kMaxDevices] = {};
+  const int dev = lmoe::current_device_index();
+  if (dev < 0) return 1;
+  if (n_of[dev] == 0) {
+    int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+    n_of[dev] = n > 0 ? n : 1;
   }
-  return n;
+  return n_of[dev];
 }
 
 }  // namespace

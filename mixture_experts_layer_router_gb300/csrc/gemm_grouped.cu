@@ -9,13 +9,15 @@ template <int MODE, bool F8>
 static cudaError_t launch_grouped_impl(const CUtensorMap& tok, const CUtensorMap& w0,
                                        const CUtensorMap& w1, const GroupedArgs& a, int grid,
                                        cudaStream_t s) {
-  static bool smem_set = false;
-  if (!smem_set) {
+  static bool smem_set[kMaxDevices] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(gemm_grouped_kernel<MODE, F8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kGSmemBytes);
     if (e != cudaSuccess) return e;
-    smem_set = true;
+    smem_set[dev] = true;
   }
   gemm_grouped_kernel<MODE, F8><<<grid, kGThreads, kGSmemBytes, s>>>(tok, w0, w1, a);
   return cudaGetLastError();

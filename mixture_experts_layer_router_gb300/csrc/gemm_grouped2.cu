@@ -10,7 +10,10 @@ template <int MODE, bool F8>
 static cudaError_t launch_pair_impl(const CUtensorMap& tok, const CUtensorMap& w0,
                                     const CUtensorMap& w1, const GroupedArgs& a, int sms,
                                     cudaStream_t s) {
-  static int max_clusters = 0;
+  static int max_clusters_of[kMaxDevices] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int& max_clusters = max_clusters_of[dev];
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];

@@ -11,6 +11,16 @@
 
 namespace lmoe {
 
+// Kernel attributes (the dynamic shared-memory limit) and occupancy answers
+// belong to a device: launchers keep one "done" flag per device ordinal.
+// Setting an attribute twice from racing threads is harmless.
+constexpr int kMaxDevices = 64;
+inline int current_device_index() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
 struct GemmMaps {
   CUtensorMap a, b, bu, a2, b2;
 };

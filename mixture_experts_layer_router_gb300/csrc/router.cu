@@ -13,12 +13,14 @@ static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w
   if (a.stages > kRMaxStages) a.stages = kRMaxStages;
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const int smem = fixed + a.stages * per_stage;
-  static bool smem_set = false;
-  if (!smem_set) {
+  static bool smem_set[kMaxDevices] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(
         router_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRMaxSmem);
     if (e != cudaSuccess) return e;
-    smem_set = true;
+    smem_set[dev] = true;
   }
   const int m_tiles = (a.T + 127) / 128;
   const int grid = m_tiles < sms ? m_tiles : sms;
