@@ -443,10 +443,11 @@ def run_ours(args, cfg, rank, world, dist):
         "dtype": ("e4m3 GEMMs, fp32 router" if args.fp8_dense else
                   "e4m3 experts, bf16 elsewhere") if f8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) bf16 weights)",
-        "config": {**workload_config(cfg),
-                   "expert_gemm": "single-SM" if args.no_sm_pairs else "SM pairs where shapes allow",
-                   **({"capacity": args.capacity, "group_size": args.group_size,
-                       "rounds": rounds_info} if args.capacity > 0 else {})},
+        "config": workload_config(cfg),
+        "variant": {"expert_gemm": "single-SM" if args.no_sm_pairs else
+                    "SM pairs where shapes allow",
+                    **({"capacity": args.capacity, "group_size": args.group_size,
+                        "rounds": rounds_info} if args.capacity > 0 else {})},
         "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
         "tc_roofline_frac": tc_ms / ms_step,
         "layer_roofline": {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms,
