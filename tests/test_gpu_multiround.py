@@ -94,3 +94,30 @@ def test_worst_case_rounds_launch_count_and_errors():
     layer.set_capacity(0)
     with pytest.raises(capi.LatentMoEError):
         layer.rounds()
+
+
+def test_all_e4m3_rounds_and_replay_equal_one_pass():
+    """All-E4M3 GEMMs with the capacity schedule, and router replay of the
+    same choices and gates: every variant reproduces the one-pass forward
+    bit for bit (same codes, same scales, same fp32 expert outputs)."""
+    cfg = synth.LayerConfig("tiny-shared", T=300, d=256, l=512, E=8, k=3, F=512, Fs=256)
+    w = synth.make_weights(cfg, 11, "cuda")
+    x = synth.make_x(cfg, 11, "cuda")
+    layer = gh.make_layer(cfg, w, fp8=True, fp8_dense=True)
+    scales = [0.02, 0.01, 0.01, 0.005, 0.01]
+    layer.set_fp8_scales(scales)
+    y0 = layer.forward(x).clone()
+    r = layer.get_routing(cfg.T, "cuda")
+    idx, gates = r["idx"].clone(), r["gates"].clone()
+    layer.set_capacity(40, 4)
+    layer.set_fp8_scales(scales)
+    y1 = layer.forward(x).clone()
+    assert layer.rounds()["needed"] > 1
+    layer.set_fp8_scales(scales)
+    y2 = layer.forward_routed(x, idx, gates).clone()
+    layer.set_capacity(0)
+    layer.set_fp8_scales(scales)
+    y3 = layer.forward_routed(x, idx).clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(y0, y1) and torch.equal(y0, y2) and torch.equal(y0, y3)
