@@ -40,7 +40,8 @@ FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT = "expert_gate_up"
 GEMM_SRC = [os.path.join(ROOT, "mixture_experts_layer_router_gb300", "csrc", f)
-            for f in ("gemm_grouped.cuh", "gemm_grouped2.cuh")]
+            for f in ("gemm_grouped.cuh", "gemm_grouped2.cuh", "ptx.cuh", "ptx_pair.cuh",
+                      "fp8.cuh")]
 
 
 # ---------------------------------------------------------------- arithmetic

@@ -163,3 +163,26 @@ def test_fused_router_matches_standalone_routing(name, renorm):
     torch.cuda.synchronize()
     for key in ("idx", "gates", "counts", "offsets", "perm", "pos"):
         assert torch.equal(r[key], alone[key]), key
+
+
+@pytest.mark.parametrize("fp8,dense", [(False, False), (True, False), (True, True)])
+def test_single_sm_expert_shapes(fp8, dense):
+    """F = l = 384 (F % 256 and l % 512 nonzero): both expert GEMMs run the
+    single-SM kernels inside the layer; bf16 against the oracle, and the
+    E4M3 variants against their bf16 counterpart within the E4M3 error."""
+    cfg = synth.LayerConfig("odd", T=333, d=256, l=384, E=12, k=3, F=384, Fs=384)
+    w = synth.make_weights(cfg, 21, "cuda")
+    x = synth.make_x(cfg, 21, "cuda")
+    layer = gh.make_layer(cfg, w, fp8=fp8, fp8_dense=dense)
+    if not fp8:
+        _check_layer(cfg, w, x, layer)
+        return
+    layer.forward(x)
+    y = layer.forward(x)
+    r = layer.get_routing(cfg.T, "cuda")
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    W = gh.oracle_weights(w)
+    exact = ref.forward(gh.f64(x), W, cfg.k, logits=gh.f64(r["logits"]))["y"]
+    rel = np.linalg.norm(gh.f64(y) - exact) / np.linalg.norm(exact)
+    assert rel < 0.15, rel
