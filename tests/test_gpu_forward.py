@@ -186,3 +186,24 @@ def test_single_sm_expert_shapes(fp8, dense):
     exact = ref.forward(gh.f64(x), W, cfg.k, logits=gh.f64(r["logits"]))["y"]
     rel = np.linalg.norm(gh.f64(y) - exact) / np.linalg.norm(exact)
     assert rel < 0.15, rel
+
+
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_forward_host_chunks_all_e4m3_shared(out_fp32):
+    """The host-buffer forward copies y out in row chunks behind the chunked
+    up-projection (here with the E4M3 shared expert's fp32 partial): bit for
+    bit the device forward, with a ragged last chunk."""
+    cfg = synth.LayerConfig("host", T=2600, d=512, l=256, E=8, k=2, F=512, Fs=256)
+    w = synth.make_weights(cfg, 13, "cuda")
+    x = synth.make_x(cfg, 13, "cuda")
+    layer = gh.make_layer(cfg, w, out_fp32=out_fp32, fp8=True, fp8_dense=True)
+    scales = [0.02, 0.01, 0.01, 0.005, 0.01]
+    layer.set_fp8_scales(scales)
+    y_dev = layer.forward(x)
+    torch.cuda.synchronize()
+    layer.set_fp8_scales(scales)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty((cfg.T, cfg.d), dtype=y_dev.dtype).pin_memory()
+    layer.forward_host(xh, yh)
+    assert torch.equal(yh, y_dev.cpu())
+    assert layer.status() == 0
