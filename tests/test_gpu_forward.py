@@ -190,9 +190,8 @@ def test_single_sm_expert_shapes(fp8, dense):
 
 @pytest.mark.parametrize("out_fp32", [False, True])
 def test_forward_host_chunks_all_e4m3_shared(out_fp32):
-    """The host-buffer forward copies y out in row chunks behind the chunked
-    up-projection (here with the E4M3 shared expert's fp32 partial): bit for
-    bit the device forward, with a ragged last chunk."""
+    """The host-buffer forward with all-E4M3 GEMMs and a shared expert (the
+    up-projection's fp32 partial) equals the device forward bit for bit."""
     cfg = synth.LayerConfig("host", T=2600, d=512, l=256, E=8, k=2, F=512, Fs=256)
     w = synth.make_weights(cfg, 13, "cuda")
     x = synth.make_x(cfg, 13, "cuda")
