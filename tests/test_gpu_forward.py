@@ -206,3 +206,36 @@ def test_forward_host_chunks_all_e4m3_shared(out_fp32):
     layer.forward_host(xh, yh)
     assert torch.equal(yh, y_dev.cpu())
     assert layer.status() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(T=200, d=256, l=128, E=1, k=1, F=256),     # one expert: the dense SwiGLU sandwich
+    dict(T=150, d=256, l=128, E=16, k=16, F=128),   # every expert chosen: the full mixture
+    dict(T=100, d=384, l=256, E=5, k=3, F=256),     # odd expert count
+    dict(T=256, d=256, l=128, E=512, k=16, F=128),  # widest top-k at the largest E
+])
+def test_degenerate_and_extreme_routing(shape):
+    """The fused router and the rest of the layer at the edges of the routing
+    space: E = 1, k = E, odd E, and k = 16 with E = 512."""
+    cfg = synth.LayerConfig("edge", Fs=0, **shape)
+    w = synth.make_weights(cfg, 17, "cuda")
+    x = synth.make_x(cfg, 17, "cuda")
+    layer = gh.make_layer(cfg, w)
+    y, ora = _check_layer(cfg, w, x, layer)
+    if cfg.E == 1:
+        # every token in the one expert with gate 1: y = W_up SwiGLU(W_dn x)
+        W = gh.oracle_weights(w)
+        z = ref.latent_down(gh.f64(x), W.w_dn)
+        wg, wu, wd = W.expert(0)
+        dense = ref.latent_up(ref.swiglu_ffn(z, wg, wu, wd), W.w_up)
+        assert np.allclose(ora["y"], dense, rtol=0, atol=1e-12)
+    # the E4M3 path on the same edges: routing identical, output near bf16
+    layer8 = gh.make_layer(cfg, w, fp8=True, fp8_dense=True)
+    layer8.forward(x)
+    y8 = layer8.forward(x)
+    r8 = layer8.get_routing(cfg.T, "cuda")
+    torch.cuda.synchronize()
+    assert layer8.status() == 0
+    assert torch.equal(r8["idx"], layer.get_routing(cfg.T, "cuda")["idx"])
+    rel = (y8.float() - y.float()).norm() / y.float().norm()
+    assert rel < 0.15, rel.item()
