@@ -162,7 +162,9 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w);
  * with LATENTMOE_OUT_FP32). 1 <= T <= max_tokens. Asynchronous on `stream`;
  * no host synchronisation and no device-to-host copy happen inside.
  * out must not overlap x or the weights. Bitwise deterministic for fixed
- * inputs and device. */
+ * inputs and device. Nothing in it synchronises the host, so it can be
+ * captured into a CUDA graph once a first call outside the capture has set
+ * up the kernels on the device. */
 int latentmoe_forward(latentmoe_t h, const void* x, void* out, int64_t T,
                       latentmoe_stream_t stream);
 
