@@ -296,7 +296,8 @@ def run_ours(args, cfg, rank, world, dist):
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    if rank == 0 or not os.path.exists(capi.LIB_PATH):
+    # one rank builds (a no-op when the library is current); the others wait
+    if rank == 0:
         build.build()
     if dist is not None:
         dist.barrier()
