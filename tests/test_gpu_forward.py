@@ -275,3 +275,27 @@ def test_forward_captures_into_a_cuda_graph(fp8):
         torch.cuda.synchronize()
         assert torch.equal(y, eager[i]), i
     assert layer.status() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_reloading_weights_matches_a_fresh_handle(fp8):
+    """load_weights twice on one handle (the owned copy, packed tiles and
+    E4M3 scales rebuilt) gives the same output as a new handle."""
+    cfg = synth.CONFIGS["tiny"]
+    wa = synth.make_weights(cfg, 31, "cuda")
+    wb = synth.make_weights(cfg, 32, "cuda")
+    x = synth.make_x(cfg, 31, "cuda")
+    scales = [0.02, 0.01, 0.01, 0.005, 0.01]
+    layer = gh.make_layer(cfg, wa, fp8=fp8, fp8_dense=fp8)
+    layer.forward(x)
+    layer.load_weights(wb)
+    if fp8:
+        layer.set_fp8_scales(scales)
+    y1 = layer.forward(x).clone()
+    fresh = gh.make_layer(cfg, wb, fp8=fp8, fp8_dense=fp8)
+    if fp8:
+        fresh.set_fp8_scales(scales)
+        assert fresh.fp8_all_weight_scales() == layer.fp8_all_weight_scales()
+    y2 = fresh.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
