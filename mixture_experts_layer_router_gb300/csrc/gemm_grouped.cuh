@@ -274,6 +274,107 @@ __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint
   __syncwarp();
 }
 
+// One tile's epilogue for one epilogue warp, shared by the single-SM and the
+// SM-pair kernels. The warp owns TMEM lanes [32 * quarter, +32) (lane_off)
+// and the 32-token chunks half, half + 2, ... of the tile's len tokens.
+//   SwiGLU: h = SiLU(s_g acc0) * (s_u acc1) for output features
+//           [feat0, +32), written as bf16 or (F8) E4M3 codes with max |h| of the
+//           valid tokens folded into amax; TMEM is released before the stores.
+//   plain:  acc0 and acc1 (when `two`) scaled by s_w and written to features
+//           feat0 and feat1 (each only if below n_out), bf16 or fp32; TMEM is
+//           released after the stores.
+// release() hands TMEM back to the MMA issuer.
+template <int MODE, bool F8, typename Release>
+__device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint32_t tmem_lanes,
+                                                      int half, int g, int len, long long out0,
+                                                      int feat0, int feat1, bool two,
+                                                      float in_s, float out_inv, float& amax,
+                                                      uint8_t* stage_w, Release release) {
+  const int nchunks = (len + 31) / 32;
+  if constexpr (MODE == kGrpSwiglu && F8) {
+    const float sg = in_s * a.w_scale0[g], su = in_s * a.w_scale1[g];
+    uint32_t hq[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = half + 2 * i;
+      if (ch < nchunks) {
+        uint32_t gv[32], uv[32];
+        tmem_ld_32cols(tmem_lanes + ch * 32, gv);
+        tmem_ld_32cols(tmem_lanes + 256 + ch * 32, uv);
+        tmem_ld_wait();
+        const int valid = len - ch * 32;
+        float hv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          hv[j] = silu(__uint_as_float(gv[j]) * sg) * (__uint_as_float(uv[j]) * su);
+          if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          hq[i][j] =
+              quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3], out_inv);
+      }
+    }
+    release();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = half + 2 * i;
+      if (ch < nchunks) gstore_chunk_f8(a, hq[i], stage_w, out0 + ch * 32, len - ch * 32, feat0);
+    }
+  } else if constexpr (MODE == kGrpSwiglu) {
+    // h for this warp's chunks (at most 4) packed to bf16 in registers, then
+    // TMEM goes back to the MMA before the slower transposing stores
+    uint32_t hp[4][16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = half + 2 * i;
+      if (ch < nchunks) {
+        uint32_t gv[32], uv[32];
+        tmem_ld_32cols(tmem_lanes + ch * 32, gv);
+        tmem_ld_32cols(tmem_lanes + 256 + ch * 32, uv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          hp[i][j] = pack_bf16x2(silu(__uint_as_float(gv[2 * j])) * __uint_as_float(uv[2 * j]),
+                                 silu(__uint_as_float(gv[2 * j + 1])) *
+                                     __uint_as_float(uv[2 * j + 1]));
+      }
+    }
+    release();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = half + 2 * i;
+      if (ch < nchunks) gstore_chunk(a, hp[i], stage_w, out0 + ch * 32, len - ch * 32, feat0);
+    }
+  } else {
+    const float so = F8 ? in_s * a.w_scale0[g] : 1.0f;
+    for (int ch = half; ch < nchunks; ch += 2) {
+      const long long row0 = out0 + ch * 32;
+      const int valid = len - ch * 32;
+#pragma unroll 1
+      for (int acc = 0; acc < 2; ++acc) {
+        if (acc == 1 && !two) break;
+        const int feat = acc == 0 ? feat0 : feat1;
+        if (feat >= a.n_out) continue;
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_lanes + acc * 256 + ch * 32, v);
+        tmem_ld_wait();
+        if (a.out_f32) {
+          gstore_chunk_f32(a, v, so, row0, valid, feat);
+          continue;
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          o[j] =
+              pack_bf16x2(__uint_as_float(v[2 * j]) * so, __uint_as_float(v[2 * j + 1]) * so);
+        gstore_chunk(a, o, stage_w, row0, valid, feat);
+      }
+    }
+    release();
+  }
+}
+
 template <int MODE, bool F8>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_grouped_kernel(const __grid_constant__ CUtensorMap tmTok,
@@ -437,100 +538,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const bool two = second_acc_used<MODE>(a, c.f);
       if (!warp_wait_bounded(tfull_bar, acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
-      const int nchunks = (c.len + 31) / 32;
-      if constexpr (MODE == kGrpSwiglu && F8) {
-        // h = SiLU(s0 acc0) * (s1 acc1), its maximum over the valid tokens,
-        // and its E4M3 codes; TMEM goes back to the MMA before the stores
-        const float sg = in_s * a.w_scale0[c.g], su = in_s * a.w_scale1[c.g];
-        uint32_t hq[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = half + 2 * i;
-          if (ch < nchunks) {
-            uint32_t g[32], u[32];
-            tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
-            tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
-            tmem_ld_wait();
-            const int valid = c.len - ch * 32;
-            float hv[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              hv[j] = silu(__uint_as_float(g[j]) * sg) * (__uint_as_float(u[j]) * su);
-              if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              hq[i][j] = quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3],
-                                     out_inv);
-          }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(tempty_bar);
-        const int feat0 = c.f * 128 + quarter * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = half + 2 * i;
-          if (ch < nchunks)
-            gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
-                            c.len - ch * 32, feat0);
-        }
-      } else if constexpr (MODE == kGrpSwiglu) {
-        // Read both accumulators and form h = SiLU(gate) * up for this
-        // warp's chunks (at most 4), packed to bf16 in registers; then hand
-        // TMEM back to the MMA before the slower transposing stores.
-        uint32_t hp[4][16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = half + 2 * i;
-          if (ch < nchunks) {
-            uint32_t g[32], u[32];
-            tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
-            tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              hp[i][j] = pack_bf16x2(silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]),
-                                     silu(__uint_as_float(g[2 * j + 1])) *
-                                         __uint_as_float(u[2 * j + 1]));
-          }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(tempty_bar);
-        const int feat0 = c.f * 128 + quarter * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = half + 2 * i;
-          if (ch < nchunks)
-            gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
-                         c.len - ch * 32, feat0);
-        }
-      } else {
-        for (int ch = half; ch < nchunks; ch += 2) {
-          const long long tok_row0 = static_cast<long long>(c.out0) + ch * 32;
-          const int tok_valid = c.len - ch * 32;
-#pragma unroll 1
-          for (int acc = 0; acc < 2; ++acc) {
-            if (acc == 1 && !two) break;
-            uint32_t v[32];
-            tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
-            tmem_ld_wait();
-            const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
-            const int feat0 = c.f * 256 + acc * 128 + quarter * 32;
-            if (a.out_f32) {
-              if (feat0 < a.n_out) gstore_chunk_f32(a, v, so, tok_row0, tok_valid, feat0);
-              continue;
-            }
-            uint32_t o[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
-                                 __uint_as_float(v[2 * j + 1]) * so);
-            if (feat0 < a.n_out) gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
-          }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(tempty_bar);
-      }
+      const int feat0 =
+          MODE == kGrpSwiglu ? c.f * 128 + quarter * 32 : c.f * 256 + quarter * 32;
+      grouped_tile_epilogue<MODE, F8>(a, tmem_base + lane_off, half, c.g, c.len, c.out0, feat0,
+                                      feat0 + 128, two, in_s, out_inv, amax, stage_w, [&] {
+                                        tc_fence_before_sync();
+                                        mbar_arrive(tempty_bar);
+                                      });
       acc_phase ^= 1u;
     }
     if constexpr (F8 && MODE == kGrpSwiglu) {

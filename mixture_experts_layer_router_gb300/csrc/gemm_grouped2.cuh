@@ -243,99 +243,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const PTile c = decode_ptile(t, a, gt);
       if (!warp_wait_bounded_pair(tfull_bar, acc_phase, abort_flag, peer_abort, a.status)) break;
       tc_fence_after_sync();
-      const int nchunks = (c.len + 31) / 32;
-      if constexpr (MODE == kGrpSwiglu) {
-        const int fblock = 2 * c.p + static_cast<int>(rank);
-        const int feat0 = fblock * 128 + quarter * 32;
-        if constexpr (F8) {
-          const float sg = in_s * a.w_scale0[c.g], su = in_s * a.w_scale1[c.g];
-          uint32_t hq[4][8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = half + 2 * i;
-            if (ch < nchunks) {
-              uint32_t g[32], u[32];
-              tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
-              tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
-              tmem_ld_wait();
-              const int valid = c.len - ch * 32;
-              float hv[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                hv[j] = silu(__uint_as_float(g[j]) * sg) * (__uint_as_float(u[j]) * su);
-                if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
-              }
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                hq[i][j] = quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3],
-                                       out_inv);
-            }
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty_leader);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = half + 2 * i;
-            if (ch < nchunks)
-              gstore_chunk_f8(a, hq[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
-                              c.len - ch * 32, feat0);
-          }
-        } else {
-          uint32_t hp[4][16];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = half + 2 * i;
-            if (ch < nchunks) {
-              uint32_t g[32], u[32];
-              tmem_ld_32cols(tmem_base + lane_off + ch * 32, g);
-              tmem_ld_32cols(tmem_base + lane_off + 256 + ch * 32, u);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                hp[i][j] = pack_bf16x2(
-                    silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]),
-                    silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
-            }
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty_leader);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = half + 2 * i;
-            if (ch < nchunks)
-              gstore_chunk(a, hp[i], stage_w, static_cast<long long>(c.out0) + ch * 32,
-                           c.len - ch * 32, feat0);
-          }
-        }
-      } else {
-        const float so = F8 ? in_s * a.w_scale0[c.g] : 1.0f;
-        for (int ch = half; ch < nchunks; ch += 2) {
-          const long long tok_row0 = static_cast<long long>(c.out0) + ch * 32;
-          const int tok_valid = c.len - ch * 32;
-#pragma unroll 1
-          for (int acc = 0; acc < 2; ++acc) {
-            uint32_t v[32];
-            tmem_ld_32cols(tmem_base + lane_off + acc * 256 + ch * 32, v);
-            tmem_ld_wait();
-            const int feat0 = c.p * 512 + acc * 256 + static_cast<int>(rank) * 128 + quarter * 32;
-            if (a.out_f32) {
-              gstore_chunk_f32(a, v, so, tok_row0, tok_valid, feat0);
-              continue;
-            }
-            uint32_t o[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * so,
-                                 __uint_as_float(v[2 * j + 1]) * so);
-            gstore_chunk(a, o, stage_w, tok_row0, tok_valid, feat0);
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_leader);
-      }
+      const int r = static_cast<int>(rank);
+      const int feat0 = MODE == kGrpSwiglu ? (2 * c.p + r) * 128 + quarter * 32
+                                           : c.p * 512 + r * 128 + quarter * 32;
+      grouped_tile_epilogue<MODE, F8>(a, tmem_base + lane_off, half, c.g, c.len, c.out0, feat0,
+                                      feat0 + 256, true, in_s, out_inv, amax, stage_w, [&] {
+                                        // one arrival per warp on the leader's barrier
+                                        tc_fence_before_sync();
+                                        __syncwarp();
+                                        if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                                      });
       acc_phase ^= 1u;
     }
     if constexpr (F8 && MODE == kGrpSwiglu) {
