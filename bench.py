@@ -122,7 +122,7 @@ def max_over_ranks(value: float, dist, device="cpu") -> float:
 class ClockSampler:
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,clocks.mem,clocks.max.mem")
 
     def __init__(self, index: int):
         self.index = index
@@ -149,14 +149,15 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.file.seek(0)
-        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.count(",") >= 7]
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.count(",") >= 9]
         os.unlink(self.file.name)
         samples = []
         for r in rows:
             try:
                 whole, _, frac = r[0].partition(".")
                 ts = time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + float("0." + (frac or "0"))
-                samples.append((ts, float(r[1]), float(r[2]), r[4:8]))
+                samples.append((ts, float(r[1]), float(r[2]), r[4:8], float(r[3]), float(r[8]),
+                                float(r[9])))
             except Exception:
                 continue
         inside = [s for s in samples if t0 <= s[0] <= t1]
@@ -168,8 +169,12 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3])
                           if v.strip().lower() == "active"})
+        mem = sorted(s[5] for s in inside)
+        watts = sorted(s[4] for s in inside)
         return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(s[2] for s in inside),
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside),
+                "mem_mhz": mem[len(mem) // 2], "mem_max_mhz": max(s[6] for s in inside),
+                "power_w": watts[len(watts) // 2]}
 
 
 # ---------------------------------------------------------------- oracle legs
