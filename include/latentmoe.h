@@ -369,9 +369,10 @@ const char* latentmoe_strerror(int code);
  * M >= 1, K and N multiples of 128 (mode 1: N >= 1). Grouped variant: rows
  * of A and C are split by device int32 offsets [G+1] (offsets[0] = 0,
  * non-decreasing, offsets[G] <= M, G <= 512); group g multiplies with rows
- * [g*N, (g+1)*N) of B (of each half of B in mode 2). In the grouped
- * variant, mode | 4 runs the SM-pair kernel (modes 0 and 2; N % 512 == 0
- * in mode 0, N % 256 == 0 in mode 2).
+ * [g*N, (g+1)*N) of B (of each half of B in mode 2). mode | 4 runs the
+ * SM-pair kernel (tcgen05 cta_group::2 on clusters of two CTAs): in the
+ * dense entry for every mode, in the grouped variant for modes 0 and 2
+ * (N % 512 == 0 in mode 0, N % 256 == 0 in mode 2).
  * Asynchronous on `stream`; errors as above. */
 int latentmoe_debug_gemm(const void* A, const void* B, void* C, int64_t M,
                          int64_t N, int64_t K, int mode,

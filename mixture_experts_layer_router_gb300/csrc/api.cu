@@ -169,7 +169,7 @@ struct latentmoe {
   float* w_scale = nullptr;     // E4M3: [3E] scales of W_g, W_u, W_d per expert (in wmem)
   lmoe::Fp8State* f8 = nullptr; // E4M3: delayed-scaling state (in ws)
   void* wmem = nullptr;          // one allocation holding every weight copy
-  GemmMaps m_router, m_down, m_shared, m_up;
+  GemmMaps m_down, m_shared, m_up;  // dense GEMM maps (every box 128 rows)
   CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
   CUtensorMap m_wr32;            // router weights in 32-column boxes (router kernel)
   // workspace
@@ -229,6 +229,9 @@ int dense_grid(const latentmoe* h, int M, int n_tiles) {
 }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// SMs offered to the SM-pair dense GEMM kernel (0: the one-SM kernel).
+int dense_pair_sms(const latentmoe* h) { return h->sm_pairs ? h->sms : 0; }
 
 void record(latentmoe* h, int slot_base, int i, cudaStream_t s) {
   if (h->prof_slots > 0) cudaEventRecord(h->events[slot_base + i], s);
@@ -632,34 +635,32 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   LMOE_CK(h, cudaDeviceSynchronize());
 
   bool ok = true;
-  ok &= make_map(&h->m_router.b, o.w_r, E, dd, dd, 256);
   ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);
   if (h->fp8_dense)
-    ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 256);
+    ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 128);
   else
-    ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 256);
+    ok &= make_map(&h->m_down.b, o.w_dn, l, dd, dd, 128);
   // tiles of 128 rows x 128 bytes
   ok &= make_tile_map(&h->m_wg, o.w_g, E * F / 128 * (l * eb / 128), h->fp8);
   ok &= make_tile_map(&h->m_wu, o.w_u, E * F / 128 * (l * eb / 128), h->fp8);
   ok &= make_tile_map(&h->m_wd, o.w_d, E * l / 128 * (F * eb / 128), h->fp8);
   if (h->fp8_dense) {
-    ok &= make_map_u8(&h->m_up.b, o.w_up, dd, l, l, 256);
+    ok &= make_map_u8(&h->m_up.b, o.w_up, dd, l, l, 128);
     if (shared) {
       ok &= make_map_u8(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
       ok &= make_map_u8(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
-      ok &= make_map_u8(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
+      ok &= make_map_u8(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 128);
     }
   } else {
-    ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 256);
+    ok &= make_map(&h->m_up.b, o.w_up, dd, l, l, 128);
     if (shared) {
       ok &= make_map(&h->m_shared.b, o.w_gs, Fs, dd, dd, 128);
       ok &= make_map(&h->m_shared.bu, o.w_us, Fs, dd, dd, 128);
-      ok &= make_map(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 256);
+      ok &= make_map(&h->m_up.b2, o.w_ds, dd, Fs, Fs, 128);
     }
   }
   if (!ok) return LATENTMOE_ERR_CUDA;
   // unused map slots still travel as kernel parameters: give them a valid copy
-  h->m_router.bu = h->m_router.a2 = h->m_router.b2 = h->m_router.b;
   h->m_down.bu = h->m_down.a2 = h->m_down.b2 = h->m_down.b;
   if (shared) {
     h->m_shared.a2 = h->m_shared.b2 = h->m_shared.b;
@@ -776,9 +777,10 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       a.a_scale = &h->f8->scale[2];
       a.b_scale = &h->dw_scale[0];
       LMOE_CK(h, lmoe::launch_gemm_scatter_f8(m, a, dense_grid(h, Ti, a.n_tiles), s,
-                                              h->fp8_dense));
+                                              h->fp8_dense, dense_pair_sms(h)));
     } else {
-      LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s));
+      LMOE_CK(h, lmoe::launch_gemm_scatter(m, a, dense_grid(h, Ti, a.n_tiles), s,
+                                           dense_pair_sms(h)));
     }
     h->launches += 1;
   }
@@ -832,7 +834,8 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       a.out_scale = &h->f8->scale[4];
       a.out_amax = &h->f8->amax[4];
     }
-    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, dense_grid(h, Ti, a.n_tiles), s, h->fp8_dense));
+    LMOE_CK(h, lmoe::launch_gemm_swiglu(m, a, dense_grid(h, Ti, a.n_tiles), s, h->fp8_dense,
+                                        dense_pair_sms(h)));
     h->launches += 1;
   }
   record(h, slot_base, 8, s);
@@ -855,7 +858,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     if (Fs > 0) {
       a.out = h->y32;
       a.ldo = dd;
-      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true));
+      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true, dense_pair_sms(h)));
       h->launches += 1;
       GemmMaps m2 = h->m_up;
       m2.a = msh;
@@ -870,16 +873,16 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       b.out = out;
       b.ldo = dd;
       if (out32)
-        LMOE_CK(h, lmoe::launch_gemm_f32(m2, b, grid, false, s, true));
+        LMOE_CK(h, lmoe::launch_gemm_f32(m2, b, grid, false, s, true, dense_pair_sms(h)));
       else
-        LMOE_CK(h, lmoe::launch_gemm_bf16(m2, b, grid, false, s, true));
+        LMOE_CK(h, lmoe::launch_gemm_bf16(m2, b, grid, false, s, true, dense_pair_sms(h)));
     } else {
       a.out = out;
       a.ldo = dd;
       if (out32)
-        LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true));
+        LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true, dense_pair_sms(h)));
       else
-        LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, false, s, true));
+        LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, false, s, true, dense_pair_sms(h)));
     }
     h->launches += 1;
   } else {
@@ -896,9 +899,9 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.ldo = dd;
     const int grid = dense_grid(h, Ti, a.n_tiles);
     if (out32)
-      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, Fs > 0, s));
+      LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, Fs > 0, s, false, dense_pair_sms(h)));
     else
-      LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, Fs > 0, s));
+      LMOE_CK(h, lmoe::launch_gemm_bf16(m, a, grid, Fs > 0, s, false, dense_pair_sms(h)));
     h->launches += 1;
   }
   record(h, slot_base, 9, s);
@@ -1278,9 +1281,10 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
   const bool pair = (mode_bits & 4) != 0;
   const int mode = mode_bits & ~4;
   if (!A || !B || !C || M < 1 || N < 1 || K < 1 || mode < 0 || mode > 2 ||
-      (pair && (offsets == nullptr || mode == 1)))
+      (pair && offsets != nullptr && mode == 1))
     return LATENTMOE_ERR_INVALID_ARG;
-  if (pair && ((mode == 2 && N % 256) || (mode == 0 && N % 512))) return LATENTMOE_ERR_UNSUPPORTED;
+  if (pair && offsets && ((mode == 2 && N % 256) || (mode == 0 && N % 512)))
+    return LATENTMOE_ERR_UNSUPPORTED;
   if (K % 128 || (mode != 1 && N % 128) || M > (1 << 30) || N > (1 << 20))
     return LATENTMOE_ERR_UNSUPPORTED;
   if (offsets && (G < 1 || G > lmoe::kMaxGroups)) return LATENTMOE_ERR_UNSUPPORTED;
@@ -1343,7 +1347,7 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
     ok &= make_map(&m.bu, static_cast<const __nv_bfloat16*>(B) + groups * N * K, groups * N, K,
                    K, 128);
   } else {
-    ok &= make_map(&m.b, B, groups * N, K, K, 256);
+    ok &= make_map(&m.b, B, groups * N, K, K, 128);
     m.bu = m.b;
   }
   if (!ok) return LATENTMOE_ERR_CUDA;
@@ -1365,10 +1369,11 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
   a.status = status;
   const long long tiles = static_cast<long long>(ceil_div(M, lmoe::kBM)) * a.n_tiles;
   const int grid = offsets ? num_sms() : static_cast<int>(tiles < num_sms() ? tiles : num_sms());
+  const int pair_sms = pair ? num_sms() : 0;
   cudaError_t e;
-  if (mode == 0) e = lmoe::launch_gemm_bf16(m, a, grid, false, s);
-  else if (mode == 1) e = lmoe::launch_gemm_f32(m, a, grid, false, s);
-  else e = lmoe::launch_gemm_swiglu(m, a, grid, s);
+  if (mode == 0) e = lmoe::launch_gemm_bf16(m, a, grid, false, s, false, pair_sms);
+  else if (mode == 1) e = lmoe::launch_gemm_f32(m, a, grid, false, s, false, pair_sms);
+  else e = lmoe::launch_gemm_swiglu(m, a, grid, s, false, pair_sms);
   return e == cudaSuccess ? LATENTMOE_OK : LATENTMOE_ERR_CUDA;
 }
 }  // namespace

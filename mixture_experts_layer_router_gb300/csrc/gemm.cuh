@@ -1,14 +1,18 @@
 // Persistent tcgen05 GEMM, D = A B^T, for every matrix product of the layer.
 //
 // A [rows, K] and B [N, K] are bf16, K-major (nn.Linear layout), read by TMA
-// into a ring of shared-memory stages with 128-byte swizzle. One thread
+// into a ring of shared-memory stages with 128-byte swizzle (every map reads
+// boxes of 128 rows; a 256-row B tile is two boxes). One thread
 // issues tcgen05.mma (M = 128, N = 256, K = 16 per instruction) into one of
-// two fp32 accumulators in tensor memory (2 x 256 columns); four epilogue
+// two fp32 accumulators in tensor memory (2 x 256 columns); eight epilogue
 // warps drain the other accumulator meanwhile, apply the epilogue and store.
 //
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warps 2..5  epilogue; warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32)
+//   warps 2..9  epilogue; warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32)
+//               and every other 32-column chunk (warps 2..5 the even ones),
+//               so two warps share the stores of each row quarter (the
+//               scatter epilogue writes each row k times)
 //
 // Tiles: dense GEMMs walk (m, n) in bands of `group_m` m-tiles so that
 // concurrent CTAs share A rows and B columns in L2. Grouped GEMMs (the
@@ -64,7 +68,8 @@ constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kBTileBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kMaxGroups = 512;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kGemmEpiWarps;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kBarrierBytes = 8 * (2 * kStages + 2 + 2 + 1);
 // Epilogue staging: per epilogue warp, 32 rows x 64 bytes of bf16 output with
@@ -73,7 +78,7 @@ constexpr int kStagePitch = 80;
 constexpr int kStageWarpBytes = 32 * kStagePitch;
 constexpr int kGemmSmemBytes =
     1024 /* alignment slack */ + kStages * kStageBytes + kBarrierBytes + 16 +
-    2 * (kMaxGroups + 1) * 4 + 4 * kStageWarpBytes;
+    2 * (kMaxGroups + 1) * 4 + kGemmEpiWarps * kStageWarpBytes;
 
 struct GemmArgs {
   int grouped;             // 0: dense rows [0, M); 1: segments from seg_offsets
@@ -294,6 +299,91 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&
   }
 }
 
+// The epilogue of one tile for the calling warp: TMEM lanes [32 * quarter,
+// +32) of the accumulator at tbase hold rows row0 + 32 * quarter + lane of
+// the tile (rows valid rows from row0; fewer, or none, at the ragged end),
+// columns n_tile * 256 (SwiGLU: gate in the first 128 columns, up in the
+// last 128, output features n_tile * 128). The warp takes the 32-column
+// chunks ch = half, half + 2, ... Shared by the one-SM and the SM-pair
+// kernels, which differ only in how they hand TMEM back.
+template <int MODE, bool F8>
+__device__ __forceinline__ void dense_tile_epilogue(const GemmArgs& a, uint32_t tbase, int row0,
+                                                    int rows, int n_tile, int quarter, int half,
+                                                    uint8_t* stage_w, float acc_s, float acc_s2,
+                                                    float out_inv, float& amax) {
+  constexpr bool kSwiglu = MODE == kEpiSwiglu || MODE == kEpiSwigluF8;
+  const int lane = threadIdx.x & 31;
+  const int r = quarter * 32 + lane;
+  const bool row_ok = r < rows;
+  const long long row = static_cast<long long>(row0) + r;
+  const long long warp_row0 = static_cast<long long>(row0) + quarter * 32;
+  const int warp_rows = rows - quarter * 32;
+  if constexpr (kSwiglu) {
+#pragma unroll 1
+    for (int ch = half; ch < kBN / 64; ch += 2) {
+      uint32_t g[32], u[32];
+      tmem_ld_32cols(tbase + ch * 32, g);
+      tmem_ld_32cols(tbase + kBN / 2 + ch * 32, u);
+      tmem_ld_wait();
+      const int col = n_tile * (kBN / 2) + ch * 32;
+      if (col < a.N) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          g[i] = __float_as_uint(silu(__uint_as_float(g[i]) * acc_s) *
+                                 (__uint_as_float(u[i]) * acc_s2));
+        if constexpr (MODE == kEpiSwigluF8) {
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(g[i])));
+          }
+          store_chunk_f8_scatter(a, g, out_inv, stage_w, warp_row0, warp_rows, col);
+        } else {
+          store_chunk_bf16_staged<kEpiBf16>(a, g, stage_w, warp_row0, warp_rows, col);
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int ch = half; ch < kBN / 32; ch += 2) {
+      uint32_t v[32];
+      tmem_ld_32cols(tbase + ch * 32, v);
+      tmem_ld_wait();
+      const int col = n_tile * kBN + ch * 32;
+      if constexpr (F8) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * acc_s);
+      }
+      if constexpr (MODE == kEpiBf16 || MODE == kEpiF32) {
+        if (a.addend != nullptr && row_ok && col < a.N) {
+          // the lane's own row: 32 consecutive fp32 of the partial sum
+          const float4* src = reinterpret_cast<const float4*>(a.addend + row * a.ld_add + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = src[q];
+            v[4 * q + 0] = __float_as_uint(__uint_as_float(v[4 * q + 0]) + f.x);
+            v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + f.y);
+            v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + f.z);
+            v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + f.w);
+          }
+        }
+      }
+      if constexpr (MODE == kEpiF32) {
+        if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
+      } else if constexpr (MODE == kEpiScatterF8) {
+        if (col < a.N) {
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(v[i])));
+          }
+          store_chunk_f8_scatter(a, v, out_inv, stage_w, warp_row0, warp_rows, col);
+        }
+      } else {
+        if (col < a.N) store_chunk_bf16_staged<MODE>(a, v, stage_w, warp_row0, warp_rows, col);
+      }
+    }
+  }
+}
+
 template <int MODE, bool DUAL, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -328,7 +418,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 128);
+      mbar_init(&tempty_bar[b], 32 * kGemmEpiWarps);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -404,16 +494,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!DUAL || kb < a.kb1) {
             const int kc = kb * kKB;
             tma_load_2d(&tmA, &full_bar[stage], sa, kc, c.row0, pol);
-            if (kSwiglu) {
-              tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
+            // B in two 128-row boxes: gate and up rows of the same features
+            // (SwiGLU), or rows brow and brow + 128
+            tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
+            if (kSwiglu)
               tma_load_2d(&tmBu, &full_bar[stage], sb + kBTileBytes / 2, kc, c.brow, pol_b);
-            } else {
-              tma_load_2d(&tmB, &full_bar[stage], sb, kc, c.brow, pol_b);
-            }
+            else
+              tma_load_2d(&tmB, &full_bar[stage], sb + kBTileBytes / 2, kc, c.brow + kBN / 2,
+                          pol_b);
           } else {
             const int kc = (kb - a.kb1) * kKB;
             tma_load_2d(&tmA2, &full_bar[stage], sa, kc, c.row0, pol);
             tma_load_2d(&tmB2, &full_bar[stage], sb, kc, c.brow, pol_b);
+            tma_load_2d(&tmB2, &full_bar[stage], sb + kBTileBytes / 2, kc, c.brow + kBN / 2, pol_b);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -477,7 +570,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
+    const int half = (warp - 2) >> 2;
     uint8_t* stage_w = stage_smem + (warp - 2) * kStageWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -493,74 +586,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after_sync();
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      const bool row_ok = r < c.rows;
-      const long long row = static_cast<long long>(c.row0) + r;
-      const long long warp_row0 = static_cast<long long>(c.row0) + quarter * 32;
-      const int warp_rows = c.rows - quarter * 32;
-      if constexpr (kSwiglu) {
-#pragma unroll 1
-        for (int ch = 0; ch < kBN / 64; ++ch) {
-          uint32_t g[32], u[32];
-          tmem_ld_32cols(tbase + ch * 32, g);
-          tmem_ld_32cols(tbase + kBN / 2 + ch * 32, u);
-          tmem_ld_wait();
-          const int col = c.n * (kBN / 2) + ch * 32;
-          if (col < a.N) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              g[i] = __float_as_uint(silu(__uint_as_float(g[i]) * acc_s) *
-                                     (__uint_as_float(u[i]) * acc_s2));
-            if constexpr (MODE == kEpiSwigluF8) {
-              if (row_ok) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(g[i])));
-              }
-              store_chunk_f8_scatter(a, g, out_inv, stage_w, warp_row0, warp_rows, col);
-            } else {
-              store_chunk_bf16_staged<kEpiBf16>(a, g, stage_w, warp_row0, warp_rows, col);
-            }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int ch = 0; ch < kBN / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld_32cols(tbase + ch * 32, v);
-          tmem_ld_wait();
-          const int col = c.n * kBN + ch * 32;
-          if constexpr (F8) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * acc_s);
-          }
-          if constexpr (MODE == kEpiBf16 || MODE == kEpiF32) {
-            if (a.addend != nullptr && row_ok && col < a.N) {
-              // the lane's own row: 32 consecutive fp32 of the partial sum
-              const float4* src = reinterpret_cast<const float4*>(a.addend + row * a.ld_add + col);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 f = src[q];
-                v[4 * q + 0] = __float_as_uint(__uint_as_float(v[4 * q + 0]) + f.x);
-                v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + f.y);
-                v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + f.z);
-                v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + f.w);
-              }
-            }
-          }
-          if constexpr (MODE == kEpiF32) {
-            if (row_ok && col < a.N) store_chunk<MODE>(a, v, row, col);
-          } else if constexpr (MODE == kEpiScatterF8) {
-            if (col < a.N) {
-              if (row_ok) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(v[i])));
-              }
-              store_chunk_f8_scatter(a, v, out_inv, stage_w, warp_row0, warp_rows, col);
-            }
-          } else {
-            if (col < a.N) store_chunk_bf16_staged<MODE>(a, v, stage_w, warp_row0, warp_rows, col);
-          }
-        }
-      }
+      dense_tile_epilogue<MODE, F8>(a, tbase, c.row0, c.rows, c.n, quarter, half, stage_w, acc_s,
+                                    acc_s2, out_inv, amax);
       tc_fence_before_sync();
       mbar_arrive(&tempty_bar[acc]);
       if (++acc == 2) {

@@ -5,9 +5,9 @@
 
 namespace lmoe {
 cudaError_t launch_gemm_bf16(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
-                             cudaStream_t s, bool f8) {
-  if (f8) return launch_gemm_impl<kEpiBf16, false, true>(m, a, grid, s);
-  return dual ? launch_gemm_impl<kEpiBf16, true>(m, a, grid, s)
-              : launch_gemm_impl<kEpiBf16, false>(m, a, grid, s);
+                             cudaStream_t s, bool f8, int pair_sms) {
+  if (f8) return launch_gemm_impl<kEpiBf16, false, true>(m, a, grid, s, pair_sms);
+  return dual ? launch_gemm_impl<kEpiBf16, true>(m, a, grid, s, pair_sms)
+              : launch_gemm_impl<kEpiBf16, false>(m, a, grid, s, pair_sms);
 }
 }  // namespace lmoe

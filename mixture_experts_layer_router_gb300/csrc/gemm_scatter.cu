@@ -3,7 +3,8 @@
 #include "gemm_launch.cuh"
 
 namespace lmoe {
-cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s) {
-  return launch_gemm_impl<kEpiScatter, false>(m, a, grid, s);
+cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s,
+                                int pair_sms) {
+  return launch_gemm_impl<kEpiScatter, false>(m, a, grid, s, pair_sms);
 }
 }  // namespace lmoe

@@ -5,8 +5,8 @@
 
 namespace lmoe {
 cudaError_t launch_gemm_scatter_f8(const GemmMaps& m, const GemmArgs& a, int grid,
-                                   cudaStream_t s, bool f8) {
-  if (f8) return launch_gemm_impl<kEpiScatterF8, false, true>(m, a, grid, s);
-  return launch_gemm_impl<kEpiScatterF8, false>(m, a, grid, s);
+                                   cudaStream_t s, bool f8, int pair_sms) {
+  if (f8) return launch_gemm_impl<kEpiScatterF8, false, true>(m, a, grid, s, pair_sms);
+  return launch_gemm_impl<kEpiScatterF8, false>(m, a, grid, s, pair_sms);
 }
 }  // namespace lmoe

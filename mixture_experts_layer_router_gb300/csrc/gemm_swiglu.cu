@@ -4,8 +4,8 @@
 
 namespace lmoe {
 cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s,
-                               bool f8) {
-  if (f8) return launch_gemm_impl<kEpiSwigluF8, false, true>(m, a, grid, s);
-  return launch_gemm_impl<kEpiSwiglu, false>(m, a, grid, s);
+                               bool f8, int pair_sms) {
+  if (f8) return launch_gemm_impl<kEpiSwigluF8, false, true>(m, a, grid, s, pair_sms);
+  return launch_gemm_impl<kEpiSwiglu, false>(m, a, grid, s, pair_sms);
 }
 }  // namespace lmoe

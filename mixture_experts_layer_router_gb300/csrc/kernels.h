@@ -26,19 +26,22 @@ struct GemmMaps {
 };
 
 // One launch of gemm_tc_kernel<MODE, DUAL, F8>; `grid` persistent CTAs.
-// f8: E4M3 operands (a_scale, b_scale set; not with dual).
+// f8: E4M3 operands (a_scale, b_scale set; not with dual). pair_sms > 0 (dense
+// GEMMs only): the SM-pair kernel instead, on up to pair_sms / 2 clusters of
+// two CTAs (fewer if fewer are resident at once or there are fewer tiles).
 cudaError_t launch_gemm_bf16(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
-                             cudaStream_t s, bool f8 = false);
+                             cudaStream_t s, bool f8 = false, int pair_sms = 0);
 cudaError_t launch_gemm_f32(const GemmMaps& m, const GemmArgs& a, int grid, bool dual,
-                            cudaStream_t s, bool f8 = false);
+                            cudaStream_t s, bool f8 = false, int pair_sms = 0);
 // SwiGLU epilogue; with f8 the output is E4M3 codes (out_scale, out_amax,
 // b_scale2 set).
 cudaError_t launch_gemm_swiglu(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s,
-                               bool f8 = false);
-cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
+                               bool f8 = false, int pair_sms = 0);
+cudaError_t launch_gemm_scatter(const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t s,
+                                int pair_sms = 0);
 // kEpiScatterF8: the scatter with E4M3 output (out_scale, out_amax set).
 cudaError_t launch_gemm_scatter_f8(const GemmMaps& m, const GemmArgs& a, int grid,
-                                   cudaStream_t s, bool f8 = false);
+                                   cudaStream_t s, bool f8 = false, int pair_sms = 0);
 
 // One launch of gemm_grouped_kernel<mode, f8> (kGrpSwiglu or kGrpPlain;
 // bf16 or E4M3 operands): tok = token rows (64-row boxes), w0/w1 = packed

@@ -120,3 +120,60 @@ def test_set_sm_pairs_rejects_bad_values():
     assert lib.latentmoe_set_sm_pairs(None, 1) == capi.ERR_INVALID_ARG
     layer.set_sm_pairs(False)
     layer.set_sm_pairs(True)
+
+
+# ---------------------------------------------------------------- dense GEMMs
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (300, 384, 256), (1000, 1024, 512),
+                                   (4096, 256, 1024), (513, 128, 384)])
+def test_pair_dense_equals_single_sm(mode, M, N, K):
+    """The dense SM-pair kernel (M = 256 pair tiles; ragged last tile, whose
+    second CTA may hold no rows) agrees bit for bit with the one-SM kernel."""
+    gh.lib()
+    A = _rand((M, K), 11)
+    B = _rand(((2 if mode == 2 else 1) * N, K), 12, 0.05)
+    dt = torch.float32 if mode == 1 else torch.bfloat16
+    C1 = torch.full((M, N), 3.0, dtype=dt, device="cuda")
+    C2 = torch.full((M, N), -3.0, dtype=dt, device="cuda")
+    assert capi.debug_gemm(A, B, C1, M, N, K, mode) == capi.OK
+    assert capi.debug_gemm(A, B, C2, M, N, K, mode | PAIR) == capi.OK
+    torch.cuda.synchronize()
+    assert capi.debug_status() == 0
+    assert torch.equal(C1, C2)
+    Ad, Bd = A.double().cpu(), B.double().cpu()
+    if mode == 2:
+        gate, up = Ad @ Bd[:N].T, Ad @ Bd[N:].T
+        want = gate / (1 + torch.exp(-gate)) * up
+    else:
+        want = Ad @ Bd.T
+    err = (C2.double().cpu() - want).abs()
+    assert (err <= want.abs() * 2 ** -7 + 1e-3 * want.abs().max()).all()
+
+
+SHARED = synth.LayerConfig("shared-ragged", T=300, d=512, l=256, E=16, k=2, F=256, Fs=512)
+
+
+@pytest.mark.parametrize("fp8_dense", [False, True])
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_layer_dense_pairs_on_and_off(fp8_dense, out_fp32):
+    """Every dense GEMM of the forward (the scatter down-projection, the
+    shared expert's SwiGLU, the up-projection with the shared down-projection,
+    fp32 output, E4M3 operands) gives the same output on SM pairs."""
+    cfg = SHARED
+    w = synth.make_weights(cfg, 5, "cuda")
+    x = synth.make_x(cfg, 5, "cuda")
+    layer = gh.make_layer(cfg, w, out_fp32=out_fp32, fp8=fp8_dense, fp8_dense=fp8_dense)
+    outs = []
+    for pairs in (False, True):
+        layer.set_sm_pairs(pairs)
+        if fp8_dense:
+            layer.set_fp8_scales([0.02, 0.01, 0.03, 0.02, 0.01])
+        outs.append(layer.forward(x).clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(outs[0], outs[1])
+    if not fp8_dense:
+        r = layer.get_routing(cfg.T, "cuda")
+        ora = ref.forward(gh.f64(x), gh.oracle_weights(w), cfg.k, logits=gh.f64(r["logits"]))
+        gh.assert_y_close(outs[1], ora["y"])
