@@ -67,6 +67,15 @@ CONFIGS: Dict[str, LayerConfig] = {
     # full-width shared expert: the profiler proxy for that shape.
     "mai-base-2-slice": LayerConfig("mai-base-2-slice", T=512, d=8704, l=4096,
                                     E=16, k=7, F=10240, Fs=10240),
+    # MAI-Base-1's dense GEMMs at full size (T=16384, d=6656, l=3072) with 8
+    # tiny experts (F=256, every token on all of them): ~3 GB on the device,
+    # the profiler proxy for the down- and up-projection kernels.
+    "mai-base-1-dense": LayerConfig("mai-base-1-dense", T=16384, d=6656, l=3072, E=8, k=8,
+                                    F=256),
+    # The same for the MAI-Base-2-like layer with its full-width shared expert
+    # (T=8192, d=8704, l=4096, F_s=10240).
+    "mai-base-2-dense": LayerConfig("mai-base-2-dense", T=8192, d=8704, l=4096, E=8, k=7,
+                                    F=256, Fs=10240),
     # The MAI-Base-1 router at full size (T=16384, d=6656, E=512, top-8) with
     # 128-wide experts: the profiler proxy for the router kernel alone.
     "mai-base-1-router": LayerConfig("mai-base-1-router", T=16384, d=6656, l=128,
