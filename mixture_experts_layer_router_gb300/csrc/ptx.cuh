@@ -18,6 +18,11 @@ constexpr unsigned kStatusTimeout = 1u;    // LATENTMOE_STATUS_TIMEOUT
 constexpr unsigned kStatusBadExpert = 2u;  // LATENTMOE_STATUS_BAD_EXPERT
 constexpr unsigned kStatusRounds = 4u;     // LATENTMOE_STATUS_ROUNDS
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
+// Suspend-time hint of every try_wait: a waiting thread may sleep up to this
+// long (it wakes as soon as the phase completes) instead of returning to the
+// poll loop, so idle roles issue fewer instructions (less power under the
+// power cap).
+constexpr uint32_t kWaitHintNs = 20000;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,10 +62,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
       : "memory");
   return done != 0;
 }
