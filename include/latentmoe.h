@@ -343,11 +343,15 @@ int latentmoe_set_capacity(latentmoe_t h, int64_t capacity, int64_t group_size,
  * of each expert in each round. UNSUPPORTED when no capacity is set. */
 int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info);
 
-/* Expert GEMMs on SM pairs (enable = 1, the default) or on single SMs (0).
- * The pair kernels run tcgen05 MMAs with M = 256 over two SMs of a cluster,
- * each SM holding half of the token tile; they are used where the shapes
- * allow (gate+up: F % 256 == 0; down: l % 512 == 0) and the single-SM
- * kernels elsewhere. Takes effect at the next forward. */
+/* GEMMs on SM pairs (enable = 1, the default) or on single SMs (0). The pair
+ * kernels run tcgen05 MMAs with M = 256 over two SMs of a cluster.
+ * - Expert GEMMs: each SM holds its weight rows and half of the token tile;
+ *   used where the shapes allow (gate+up: F % 256 == 0; down: l % 512 ==
+ *   0), the single-SM kernels elsewhere.
+ * - Dense GEMMs (down-projection, shared expert, up-projection): pair tiles
+ *   of 256 token rows, each SM holding its 128 rows and half of the weight
+ *   tile.
+ * Results are bitwise the same either way. Takes effect at the next forward. */
 int latentmoe_set_sm_pairs(latentmoe_t h, int enable);
 
 /* Kernel launches issued by this handle since creation. */
