@@ -94,3 +94,25 @@ def test_strings_and_stages(lib):
                      "expert_down", "combine", "shared_gate_up", "up_proj",
                      "fp8_scales"]
     assert lib.latentmoe_stage_name(n) is None
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: with the library absent, loading it and creating a
+    layer raise instead of computing anything."""
+    import subprocess
+    import sys
+    code = (
+        "import mixture_experts_layer_router_gb300.capi as c\n"
+        "c._lib = None\n"
+        "c.load.__defaults__ = ('/nonexistent/liblatentmoe.so',)\n"
+        "try:\n"
+        "    c.LatentMoE(256, 128, 16, 2, 256)\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', e)\n"
+        "    raise SystemExit(3)\n"
+        "raise SystemExit(0)\n")
+    root = os.path.dirname(os.path.dirname(__file__))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 3, r.stdout + r.stderr
+    assert "is missing" in r.stdout
