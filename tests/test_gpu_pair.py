@@ -177,3 +177,24 @@ def test_layer_dense_pairs_on_and_off(fp8_dense, out_fp32):
         r = layer.get_routing(cfg.T, "cuda")
         ora = ref.forward(gh.f64(x), gh.oracle_weights(w), cfg.k, logits=gh.f64(r["logits"]))
         gh.assert_y_close(outs[1], ora["y"])
+
+
+@pytest.mark.parametrize("T", [129, 256, 257, 383, 511, 600])
+def test_layer_ragged_tokens_across_pair_tiles(T):
+    """Token counts around the 256-row pair tile of the dense kernels (the
+    second CTA of the last pair tile holds part of a tile, or no rows): the
+    forward matches the oracle and is bitwise the same with pairs off."""
+    cfg = synth.LayerConfig("pair-ragged", T=600, d=384, l=256, E=12, k=3, F=256, Fs=256)
+    w = synth.make_weights(cfg, 9, "cuda")
+    x = synth.make_x(cfg, 9, "cuda")[:T].contiguous()
+    layer = gh.make_layer(cfg, w)
+    outs = []
+    for pairs in (True, False):
+        layer.set_sm_pairs(pairs)
+        outs.append(layer.forward(x).clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(outs[0], outs[1])
+    r = layer.get_routing(T, "cuda")
+    ora = ref.forward(gh.f64(x), gh.oracle_weights(w), cfg.k, logits=gh.f64(r["logits"]))
+    gh.assert_y_close(outs[0], ora["y"])
