@@ -190,6 +190,7 @@ struct latentmoe {
   __nv_bfloat16* cb = nullptr;
   __nv_bfloat16* sh = nullptr;
   unsigned* status = nullptr;
+  int* tile_counter = nullptr;  // SM-pair grouped kernels: dynamic tile scheduler
   int64_t last_T = 0;
   // host-buffer forward staging
   void* x_stage = nullptr;
@@ -314,6 +315,9 @@ int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok
   }
   if (h->sm_pairs && l % 512 == 0) {
     a.fblocks = l / 512;
+    // few long tiles per pair: dynamic tile order balances the last wave
+    a.tile_counter = h->tile_counter;
+    LMOE_CK(h, cudaMemsetAsync(h->tile_counter, 0, sizeof(int), s));
     LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpPlain, h->fp8, tok, h->m_wd, h->m_wd, a,
                                               h->sms, s));
   } else {
@@ -448,6 +452,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   const size_t o_o = take(S * l * ((flags & LATENTMOE_FP8_DENSE) ? 4 : 2));
   const size_t o_c = take(T * l * 2), o_sh = take(Fs > 0 ? T * Fs * 2 : 16);
   const size_t o_status = take(16);
+  const size_t o_tcount = take(16);
   const size_t o_f8 = take(sizeof(lmoe::Fp8State));
   const size_t o_x8 = take(h->fp8_dense ? T * d.hidden : 16);
   const size_t o_y32 = take(h->fp8_dense && Fs > 0 ? T * d.hidden * 4 : 16);
@@ -474,6 +479,7 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->cb = reinterpret_cast<__nv_bfloat16*>(base + o_c);
   h->sh = reinterpret_cast<__nv_bfloat16*>(base + o_sh);
   h->status = reinterpret_cast<unsigned*>(base + o_status);
+  h->tile_counter = reinterpret_cast<int*>(base + o_tcount);
   h->f8 = reinterpret_cast<lmoe::Fp8State*>(base + o_f8);
   h->x8 = reinterpret_cast<uint8_t*>(base + o_x8);
   h->y32 = reinterpret_cast<float*>(base + o_y32);
@@ -1330,7 +1336,10 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
     cudaError_t e;
     if (pair) {
       ga.fblocks = static_cast<int>(mode == 2 ? N / 256 : N / 512);
-      e = lmoe::launch_gemm_grouped_pair(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false,
+      ga.tile_counter = reinterpret_cast<int*>(status) + 2;
+      e = cudaMemsetAsync(ga.tile_counter, 0, sizeof(int), s);
+      if (e == cudaSuccess)
+        e = lmoe::launch_gemm_grouped_pair(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false,
                                          tok, w0, w1, ga, num_sms(), s);
     } else {
       e = lmoe::launch_gemm_grouped(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false, tok,

@@ -86,6 +86,8 @@ struct GroupedArgs {
   long long ldo;
   int out_f32;             // plain: fp32 output
   unsigned* status;
+  int* tile_counter;       // SM-pair kernel: [1] zero at launch; tiles past the first
+                           // wave are taken from it (null: static round robin)
   // E4M3 variant only
   const float* w_scale0;   // [G] scale of the weights of accumulator 0, per group
   const float* w_scale1;   // [G] accumulator 1 (SwiGLU: the up rows)
