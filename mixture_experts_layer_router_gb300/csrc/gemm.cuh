@@ -327,9 +327,10 @@ __device__ __forceinline__ void dense_tile_epilogue(const GemmArgs& a, uint32_t 
       tmem_ld_wait();
       const int col = n_tile * (kBN / 2) + ch * 32;
       if (col < a.N) {
+        const float gs_half = 0.5f * acc_s;  // SiLU's halving folded into the gate scale
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          g[i] = __float_as_uint(silu(__uint_as_float(g[i]) * acc_s) *
+          g[i] = __float_as_uint(silu_from_half(__uint_as_float(g[i]) * gs_half) *
                                  (__uint_as_float(u[i]) * acc_s2));
         if constexpr (MODE == kEpiSwigluF8) {
           if (row_ok) {

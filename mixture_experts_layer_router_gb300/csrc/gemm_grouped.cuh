@@ -294,7 +294,8 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
                                                       uint8_t* stage_w, Release release) {
   const int nchunks = (len + 31) / 32;
   if constexpr (MODE == kGrpSwiglu && F8) {
-    const float sg = in_s * a.w_scale0[g], su = in_s * a.w_scale1[g];
+    // gate scale with SiLU's halving folded in (exact)
+    const float sg_half = 0.5f * (in_s * a.w_scale0[g]), su = in_s * a.w_scale1[g];
     uint32_t hq[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -308,7 +309,7 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
         float hv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          hv[j] = silu(__uint_as_float(gv[j]) * sg) * (__uint_as_float(uv[j]) * su);
+          hv[j] = silu_from_half(__uint_as_float(gv[j]) * sg_half) * (__uint_as_float(uv[j]) * su);
           if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
         }
 #pragma unroll

@@ -309,9 +309,10 @@ __device__ __forceinline__ float tanh_approx(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float silu(float a) {
-  const float h = 0.5f * a;
-  return fmaf(h, tanh_approx(h), h);
-}
+// SiLU(a) = h + h tanh(h) with h = a / 2, from h. Callers that scale the
+// accumulator anyway pass the scale times 1/2 (exact: a power of two) and
+// save the halving.
+__device__ __forceinline__ float silu_from_half(float h) { return fmaf(h, tanh_approx(h), h); }
+__device__ __forceinline__ float silu(float a) { return silu_from_half(0.5f * a); }
 
 }  // namespace lmoe
