@@ -66,13 +66,16 @@ def layer_bytes(c, touched_experts: int, eb: int = 2, db: int = 2) -> int:
 
 
 def gate_up_work(c, touched_experts: int, eb: int = 2):
-    """Per launch of the grouped gate+up GEMM: FLOPs and algorithmic bytes
-    (gate and up weights of touched experts, z rows read, h rows written;
-    eb bytes per element: 2 for bf16, 1 for E4M3)."""
+    """Per launch of the grouped gate+up GEMM: FLOPs, algorithmic bytes (the
+    gate and up weights of the experts that got tokens, eb bytes each: 2 for
+    bf16, 1 for E4M3; the z rows it reads and the h rows it writes are
+    intermediates a fused design avoids, so they are not counted) and the
+    as-built bytes (weights + z rows read + h rows written)."""
     S = c.T * c.k
     flops = 2 * S * c.l * 2 * c.F
-    nbytes = touched_experts * 2 * c.F * c.l * eb + S * c.l * eb + S * c.F * eb
-    return flops, nbytes
+    nbytes = touched_experts * 2 * c.F * c.l * eb
+    built = nbytes + S * c.l * eb + S * c.F * eb
+    return flops, nbytes, built
 
 
 def load_peaks():
@@ -294,8 +297,138 @@ def workload_config(cfg):
             "parallelism": "replicas"}
 
 
-def run_ours(args, cfg, rank, world, dist):
+def layer_roofline(cfg, touched, ms_step, peaks, peak_src, f8, fp8_dense, capped):
+    """FLOPs, algorithmic bytes and the layer's roofline fraction. The tensor
+    peak is the measured sustained one for a run the power cap held down,
+    the burst one otherwise; E4M3 FLOPs count at the nominal E4M3/bf16 ratio."""
+    flops_tok = layer_flops_per_token(cfg)
+    eb = 1 if f8 else 2
+    lbytes = layer_bytes(cfg, touched, eb, 1 if fp8_dense else 2)
+    peak_key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    bf16_peak = peaks[peak_key] * 1e12
+    router_flops = cfg.T * 2 * cfg.d * cfg.E
+    x_flops = cfg.T * expert_flops_per_token(cfg)
+    if fp8_dense:
+        x_flops = cfg.T * flops_tok - router_flops
+    o_flops = cfg.T * flops_tok - x_flops
+    tc_ms = (o_flops / bf16_peak + x_flops / (bf16_peak * (FP8_OVER_BF16 if f8 else 1.0))) * 1e3
+    hbm_ms = lbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    return {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms, "hbm_ms": hbm_ms,
+            "roofline_ms": max(tc_ms, hbm_ms), "frac": max(tc_ms, hbm_ms) / ms_step,
+            "touched_experts": touched,
+            "tensor_peak": f"{peak_src} {'sustained' if capped else 'burst'} bf16 "
+                           f"({peaks[peak_key]:.1f} TFLOP/s)",
+            "peaks": {**peaks, "source": peak_src}}
+
+
+def cpu_oracle_baseline(cfg, r, x, w, n, f8_scales=None, fp8_dense=False):
+    """The oracle on n seeded tokens of the workload (all T when n >= T),
+    routed from the GPU logits; tokens/s, with the full-T time extrapolated
+    where n < T."""
     import numpy as np
+    from mixture_experts_layer_router_gb300 import synth
+    n = min(n, cfg.T)
+    toks = synth.sample_tokens(cfg.T, n, seed=1)
+    tsel = toks.cuda()
+    L = r["logits"][tsel].double().cpu().numpy()
+    need = sorted(set(r["idx"][tsel].cpu().numpy().ravel().tolist()))
+    fetch = host_weights(cfg, w, need)
+    xs = x[tsel].float().cpu().numpy().astype(np.float64)
+    tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch, fp8_scales=f8_scales)
+    what = "all tokens" if n == cfg.T else f"{n} seeded tokens"
+    out = {"value": tps, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+           "sample": f"{what} of the {cfg.name} workload ({dt:.1f} s), float64 NumPy oracle" +
+                     ((" (E4M3 layer at the GPU's scales)" if f8_scales is not None else "")) +
+                     " routed from the GPU logits, expert weights upcast from host bf16 inside "
+                     "the timed work"}
+    if n < cfg.T:
+        out["extrapolated_s_per_forward"] = dt * cfg.T / n
+        out["extrapolation"] = (f"x T/n = x {cfg.T / n:.0f}: overstates the per-expert fixed "
+                                "costs (weight upcast), which a full-T run pays once")
+    return out
+
+
+def measure_small(cfg, args, peaks, peak_src, local, cpu_tokens):
+    """One extra workload at N = 1: the same forward through the C ABI, each
+    timed step bracketed by CUDA events after an L2 flush (a 512 MiB write),
+    then a profiled pass for the stage times; its own clock record and CPU
+    baseline. Returns the entry of the line's "configs"."""
+    import torch
+    from mixture_experts_layer_router_gb300 import capi, synth
+    w = synth.make_weights(cfg, 0, "cuda")
+    x = synth.make_x(cfg, 0, "cuda")
+    layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
+                           router_bias=w["b_r"] is not None)
+    layer.load_weights(w)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    assert layer.status() == 0, f"device status set during the {cfg.name} warm-up"
+    t0 = time.perf_counter()
+    for _ in range(5):
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    est_ms = (time.perf_counter() - t0) * 1e3 / 5
+    # enough steps for the clock sampler (>= 0.6 s of timed work)
+    steps = max(args.steps, int(600.0 / max(est_ms, 0.02)) + 1)
+    steps = min(steps, 20000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = layer.launch_count()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(stream)
+        layer.forward(x, y)
+        b.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    launches = layer.launch_count() - launches0
+    clk = clocks.stop(wall0, wall1)
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    ms_mean = sum(ms) / len(ms)
+    prof = min(steps, 200)
+    layer.set_profiling(prof)
+    for _ in range(prof):
+        flush.fill_(1)
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    stage_ms = {}
+    for s in range(prof):
+        for name, v in layer.stage_times(s).items():
+            stage_ms[name] = stage_ms.get(name, 0.0) + v / prof
+    layer.set_profiling(0)
+    status = layer.status()
+    r = layer.get_routing(cfg.T, "cuda")
+    touched = int((r["counts"] > 0).sum().item())
+    capped = bool(clk and "sw_power_cap" in clk.get("reasons", []))
+    roof = layer_roofline(cfg, touched, ms_mean, peaks, peak_src, False, False, capped)
+    cpu = cpu_oracle_baseline(cfg, r, x, w, cpu_tokens) if not args.no_cpu_baseline else None
+    out = {"workload": workload_config(cfg)["workload"], "steps": steps,
+           "ms_per_step": ms_mean, "ms_per_step_median": ms[len(ms) // 2],
+           "tokens_per_s": cfg.T / (ms_mean / 1e3),
+           "tflops": roof["flops"] / (ms_mean / 1e3) / 1e12,
+           "roofline_frac": roof["frac"], "layer_roofline": roof,
+           "l2": "flushed before every timed step (512 MiB write outside the events)",
+           "stage_ms": stage_ms, "gpu_launches_per_step": launches / steps,
+           "clocks": clk, "cpu_baseline": cpu, "device_status": status}
+    layer.close()
+    del layer, w, x, y, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+EXTRA_CONFIGS = (("tiny", 128), ("mid", 4096), ("imbalanced", 4096), ("mai-base-2", 12))
+
+
+def run_ours(args, cfg, rank, world, dist):
+    import numpy as np  # noqa: F401
     import torch
     from mixture_experts_layer_router_gb300 import build, capi, synth
 
@@ -389,40 +522,20 @@ def run_ours(args, cfg, rank, world, dist):
     # CPU baseline: the oracle on a bounded token sample, rank 0 at N=1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        from oracle import latentmoe_ref as ref  # noqa: F401
-        n = args.cpu_tokens
-        toks = synth.sample_tokens(cfg.T, n, seed=1)
-        tsel = toks.cuda()
-        L = r["logits"][tsel].double().cpu().numpy()
-        need = sorted(set(r["idx"][tsel].cpu().numpy().ravel().tolist()))
-        fetch = host_weights(cfg, w, need)
-        xs = x[tsel].float().cpu().numpy().astype(np.float64)
         scales = (layer.fp8_state()["scales"] if args.fp8_dense else
                   layer.fp8_state()["scales"][:2]) if f8 else None
-        tps, dt = oracle_tokens_per_s(cfg, xs, L, fetch, fp8_scales=scales)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-               "sample": f"{n} seeded tokens of the {cfg.name} workload ({dt:.1f} s), float64 "
-                         "NumPy oracle" + (" (E4M3 experts at the GPU's scales)" if f8 else "") +
-                         " routed from the GPU logits, expert weights upcast from host bf16 "
-                         "inside the timed work"}
+        cpu = cpu_oracle_baseline(cfg, r, x, w, args.cpu_tokens, f8_scales=scales,
+                                  fp8_dense=args.fp8_dense)
 
     peaks, peak_src = load_peaks()
     ms_step = ms_total / args.steps
     value = world * cfg.T * args.steps / (ms_total / 1e3)
-    flops_tok = layer_flops_per_token(cfg)
+    capped = clk is None or "sw_power_cap" in clk.get("reasons", [])
+    lroof = layer_roofline(cfg, touched, ms_step, peaks, peak_src, f8, args.fp8_dense, True)
+    lroof_now = layer_roofline(cfg, touched, ms_step, peaks, peak_src, f8, args.fp8_dense,
+                               capped)
     eb = 1 if f8 else 2
-    lbytes = layer_bytes(cfg, touched, eb, 1 if args.fp8_dense else 2)
-    bf16_peak = peaks["bf16_tflops_sustained"] * 1e12
-    # FLOPs at the E4M3 rate where they run in E4M3 (experts; with --fp8-dense
-    # everything but the router)
-    router_flops = cfg.T * 2 * cfg.d * cfg.E
-    x_flops = cfg.T * expert_flops_per_token(cfg)
-    if args.fp8_dense:
-        x_flops = cfg.T * flops_tok - router_flops
-    o_flops = cfg.T * flops_tok - x_flops
-    tc_ms = (o_flops / bf16_peak + x_flops / (bf16_peak * (FP8_OVER_BF16 if f8 else 1.0))) * 1e3
-    hbm_ms = lbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
-    g_flops, g_bytes = gate_up_work(cfg, touched, eb)
+    g_flops, g_bytes, g_built = gate_up_work(cfg, touched, eb)
     g_ms = stage_ms.get(DOMINANT, float("nan"))
     g_peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if f8 else 1.0)
     g_tc = g_flops / (g_peak * 1e12) * 1e3
@@ -434,11 +547,16 @@ def run_ours(args, cfg, rank, world, dist):
         roof = {"bound": "tensor", "achieved": g_flops / (g_ms / 1e3) / 1e12,
                 "peak": g_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic(cfg.name, f8)
+    traffic = profiled_traffic(cfg.name, f8)
+    roof["traffic"] = traffic
     peak_kind = ("sustained bf16 x 2 for E4M3" if f8 else "sustained bf16") \
         if roof["bound"] == "tensor" else "HBM copy"
     roof.update({"kernel": DOMINANT + ("_e4m3" if f8 else ""), "ms_per_launch": g_ms,
-                 "algorithmic_bytes": g_bytes, "flops": g_flops,
+                 "algorithmic_bytes": g_bytes,
+                 "algorithmic": "gate and up weights of the experts that got tokens",
+                 "as_built_bytes": g_built,
+                 "as_built_gbs": g_built / (g_ms / 1e3) / 1e9,
+                 "flops": g_flops,
                  "tensor_tflops": g_flops / (g_ms / 1e3) / 1e12,
                  "peak_source": f"{peak_src} ({peak_kind})"})
 
@@ -455,12 +573,9 @@ def run_ours(args, cfg, rank, world, dist):
                     "SM pairs where shapes allow",
                     **({"capacity": args.capacity, "group_size": args.group_size,
                         "rounds": rounds_info} if args.capacity > 0 else {})},
-        "tflops": cfg.T * flops_tok / (ms_step / 1e3) / 1e12,
-        "tc_roofline_frac": tc_ms / ms_step,
-        "layer_roofline": {"flops": cfg.T * flops_tok, "bytes": lbytes, "tc_ms": tc_ms,
-                           "hbm_ms": hbm_ms, "roofline_ms": max(tc_ms, hbm_ms),
-                           "frac": max(tc_ms, hbm_ms) / ms_step, "touched_experts": touched,
-                           "peaks": {**peaks, "source": peak_src}},
+        "tflops": cfg.T * layer_flops_per_token(cfg) / (ms_step / 1e3) / 1e12,
+        "tc_roofline_frac": lroof["tc_ms"] / ms_step,
+        "layer_roofline": {**lroof, "frac_at_this_runs_clock_peak": lroof_now["frac"]},
         "roofline": roof,
         "stage_ms": stage_ms,
         "gpu_launches": int(launches),
@@ -473,6 +588,17 @@ def run_ours(args, cfg, rank, world, dist):
         names = ("z", "h", "x", "c", "shared_hidden") if args.fp8_dense else ("z", "h")
         line["fp8_scales"] = {**dict(zip(names, fp8_state["scales"])),
                               "history_steps": fp8_state["steps"]}
+
+    # the other workloads, at N = 1 only (a scaling run times the headline alone)
+    if world == 1 and not args.no_extra_configs and not f8 and cfg.name == "mai-base-1" \
+            and args.capacity == 0 and not args.no_sm_pairs:
+        layer.close()
+        del layer, w, x, y, r
+        torch.cuda.empty_cache()
+        extra = {}
+        for name, n_cpu in EXTRA_CONFIGS:
+            extra[name] = measure_small(synth.CONFIGS[name], args, peaks, peak_src, local, n_cpu)
+        line["configs"] = extra
     return line
 
 
@@ -489,6 +615,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time the headline workload only (by default an N=1 bf16 run at the "
+                         "MAI-Base-1 shape also times tiny, mid, imbalanced and MAI-Base-2)")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 E4M3 expert GEMMs with delayed scaling")
     ap.add_argument("--fp8-dense", action="store_true",

@@ -150,16 +150,30 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags,
  * library copies them into memory it owns (one allocation of the weights'
  * size, freed by latentmoe_destroy or the next load) and rewrites the expert
  * weights into contiguous tiles of 128 rows x 128 bytes for its grouped
- * GEMMs (64 bf16 columns, or 128 E4M3 codes with LATENTMOE_FP8_EXPERTS).
- * Synchronises the device before and after the copy, so pending writes to
- * the caller's buffers are seen and the caller may free or reuse them as
- * soon as this returns. Errors: INVALID_ARG (NULL pointer that the dims or
- * flags need), UNSUPPORTED (pointer not 16-byte aligned), OUT_OF_MEMORY,
- * CUDA. On error the handle has no weights loaded. */
-int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w);
+ * GEMMs (64 bf16 columns, or 128 E4M3 codes with LATENTMOE_FP8_EXPERTS;
+ * the E4M3 scales and codes are computed on the device).
+ * The copies and the repacking are enqueued on `stream`: the caller's
+ * writes to its weight buffers must be complete, or ordered before
+ * `stream`. Before returning, the call synchronises `stream` (and only
+ * that stream), so the caller may free or reuse its buffers as soon as this
+ * returns. Loading again on a handle frees the earlier copy first, which
+ * waits for the device (cudaFree). Errors: INVALID_ARG (NULL pointer that
+ * the dims or flags need), UNSUPPORTED (pointer not 16-byte aligned),
+ * OUT_OF_MEMORY, CUDA. On error the handle has no weights loaded. */
+int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w,
+                           latentmoe_stream_t stream);
 
-/* The layer forward. x: device bf16 [T, d]; out: device [T, d], bf16 (fp32
- * with LATENTMOE_OUT_FP32). 1 <= T <= max_tokens. Asynchronous on `stream`;
+/* The layer forward: the computation stated at the top of this file, from
+ * "The Training and RL Infrastructure Behind MAI-Thinking-1", section "The
+ * model the systems run" (MoE row of the shape table: softmax gating of the
+ * top-k experts over the full hidden state, one shared down-projection to
+ * the latent before dispatch and one up-projection after the combine,
+ * SwiGLU experts on the latent; section "2. Numerics" for the fp32 router
+ * logits and the fp32 combine) and "MAI-Base-2: Microsoft's 2.8T base
+ * model, and whether its compute numbers add up", section "The model" (the
+ * shared expert on the full width). x: device bf16 [T, d]; out: device
+ * [T, d], bf16 (fp32 with LATENTMOE_OUT_FP32). 1 <= T <= max_tokens.
+ * Asynchronous on `stream`;
  * no host synchronisation and no device-to-host copy happen inside.
  * out must not overlap x or the weights. Bitwise deterministic for fixed
  * inputs and device. Nothing in it synchronises the host, so it can be
@@ -195,7 +209,13 @@ int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host,
 int latentmoe_destroy(latentmoe_t h);
 
 /* Routing from given logits (the router-replay hook and the integer parity
- * test): from fp32 logits [T, E] (device) computes, on `stream`,
+ * test): the softmax gating and top-k selection of "The Training and RL
+ * Infrastructure Behind MAI-Thinking-1", section "The model the systems
+ * run" (MoE row), with the stable ordering of its section "Bitwise
+ * determinism" (equal logits: the lower expert index first), and the
+ * counting sort of the slots by expert that the dropless dispatch of its
+ * section "Memory and dropless MoE" works on (token order kept inside an
+ * expert). From fp32 logits [T, E] (device) it computes, on `stream`,
  *   idx [T, k] int32, gates [T, k] fp32   (softmax over E, stable top-k)
  *   counts [E], offsets [E+1], perm [T*k], pos [T, k]   int32 (counting sort)
  * with the handle's k and LATENTMOE_RENORM flag. All outputs are device
@@ -222,7 +242,11 @@ int latentmoe_route_from_logits(latentmoe_t h, const float* logits, int64_t T,
  * LATENTMOE_ERR_UNSUPPORTED before any work is enqueued.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. All calls share the one array and it keeps the last call's
+ * capture. The looked-up address is cached per device ordinal for the rest
+ * of the process: it does not survive cudaDeviceReset (or a context other
+ * than the device's primary one), after which the module is loaded anew at
+ * another address; do not call this entry after resetting a device it has
+ * run on. All calls share the one array and it keeps the last call's
  * contents: calls whose work overlaps on the GPU (two streams, or two host
  * threads) race and must be serialised by the caller. Asynchronous on
  * `stream`. */

@@ -53,7 +53,8 @@ class latentmoe_weights(ctypes.Structure):
 SIGNATURES = {
     "latentmoe_create": (ctypes.c_int, [ctypes.POINTER(latentmoe_dims), ctypes.c_int,
                                         ctypes.c_uint32, ctypes.POINTER(_c_void_p)]),
-    "latentmoe_load_weights": (ctypes.c_int, [_c_void_p, ctypes.POINTER(latentmoe_weights)]),
+    "latentmoe_load_weights": (ctypes.c_int, [_c_void_p, ctypes.POINTER(latentmoe_weights),
+                                                _c_void_p]),
     "latentmoe_forward": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "latentmoe_forward_routed": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                                 _c_void_p, _i64, _c_void_p]),
@@ -174,11 +175,11 @@ class LatentMoE:
         except Exception:
             pass
 
-    def load_weights(self, w: Dict[str, object]) -> None:
+    def load_weights(self, w: Dict[str, object], stream=None) -> None:
         lw = latentmoe_weights(*(_ptr(w.get(n)) for n in
                                  ("w_r", "b_r", "w_dn", "w_g", "w_u", "w_d", "w_up",
                                   "w_gs", "w_us", "w_ds")))
-        check(load().latentmoe_load_weights(self.handle, ctypes.byref(lw)),
+        check(load().latentmoe_load_weights(self.handle, ctypes.byref(lw), _stream(stream)),
               "latentmoe_load_weights", self.handle)
 
     def forward(self, x, out=None, stream=None):

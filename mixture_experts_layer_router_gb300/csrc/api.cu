@@ -512,7 +512,8 @@ int latentmoe_destroy(latentmoe_t h) {
   return LATENTMOE_OK;
 }
 
-int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
+int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w,
+                           latentmoe_stream_t stream) {
   if (h == nullptr || w == nullptr) return LATENTMOE_ERR_INVALID_ARG;
   const latentmoe_dims& d = h->dims;
   const bool shared = d.shared_ffn > 0;
@@ -548,8 +549,9 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   const size_t o_gs = take(shared ? Fs * dd * db : 16), o_us = take(shared ? Fs * dd * db : 16);
   const size_t o_ds = take(shared ? dd * Fs * db : 16);
   const size_t o_dws = take(kDenseW * 4), o_dwa = take(kDenseW * 4);
-  // the caller's writes to its weights may still be in flight on any stream
-  LMOE_CK(h, cudaDeviceSynchronize());
+  // the caller's writes to its weights are complete or ordered before `s`;
+  // replacing earlier weights frees them (cudaFree waits for the device)
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   h->loaded = false;
   if (h->wmem) {
     cudaFree(h->wmem);
@@ -581,8 +583,8 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   h->w_scale = h->fp8 ? reinterpret_cast<float*>(base + o_ws) : nullptr;
   h->dw_scale = reinterpret_cast<float*>(base + o_dws);
   const auto dd2d = cudaMemcpyDeviceToDevice;
-  LMOE_CK(h, cudaMemcpy(const_cast<void*>(o.w_r), w->w_r, E * dd * 2, dd2d));
-  if (bias) LMOE_CK(h, cudaMemcpy(const_cast<float*>(o.b_r), w->b_r, E * 4, dd2d));
+  LMOE_CK(h, cudaMemcpyAsync(const_cast<void*>(o.w_r), w->w_r, E * dd * 2, dd2d, s));
+  if (bias) LMOE_CK(h, cudaMemcpyAsync(const_cast<float*>(o.b_r), w->b_r, E * 4, dd2d, s));
   {
     // dense weights: W_dn, W_up, W_gs, W_us, W_ds (the shared three only with F_s > 0)
     const void* dsrc[kDenseW] = {w->w_dn, w->w_up, w->w_gs, w->w_us, w->w_ds};
@@ -595,22 +597,22 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
     if (h->fp8_dense) {
       // s = max |W| / 448 per matrix, codes row-major (the dense GEMM's layout)
       unsigned* damax = reinterpret_cast<unsigned*>(base + o_dwa);
-      LMOE_CK(h, cudaMemset(damax, 0, kDenseW * 4));
+      LMOE_CK(h, cudaMemsetAsync(damax, 0, kDenseW * 4, s));
       for (int m = 0; m < nd; ++m)
         LMOE_CK(h, lmoe::launch_absmax_groups(static_cast<const __nv_bfloat16*>(dsrc[m]), 1,
                                               static_cast<long long>(drows[m] * dcols[m]),
-                                              damax + m, h->sms, 0));
-      LMOE_CK(h, lmoe::launch_scales_from_amax(damax, kDenseW, h->dw_scale, 0));
+                                              damax + m, h->sms, s));
+      LMOE_CK(h, lmoe::launch_scales_from_amax(damax, kDenseW, h->dw_scale, s));
       for (int m = 0; m < nd; ++m)
         LMOE_CK(h, lmoe::launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(dsrc[m]),
                                               static_cast<uint8_t*>(ddst[m]),
                                               static_cast<long long>(drows[m]),
                                               static_cast<long long>(dcols[m]),
                                               static_cast<long long>(drows[m]), h->dw_scale + m,
-                                              false, h->sms, 0));
+                                              false, h->sms, s));
     } else {
       for (int m = 0; m < nd; ++m)
-        LMOE_CK(h, cudaMemcpy(ddst[m], dsrc[m], drows[m] * dcols[m] * 2, dd2d));
+        LMOE_CK(h, cudaMemcpyAsync(ddst[m], dsrc[m], drows[m] * dcols[m] * 2, dd2d, s));
     }
   }
   typedef const __nv_bfloat16* cbf;
@@ -623,22 +625,23 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w) {
   if (h->fp8) {
     // s = max |W_e| / 448 per expert matrix, then codes in the packed layout
     unsigned* amax = reinterpret_cast<unsigned*>(base + o_wa);
-    LMOE_CK(h, cudaMemset(amax, 0, 3 * E * 4));
+    LMOE_CK(h, cudaMemsetAsync(amax, 0, 3 * E * 4, s));
     for (int m = 0; m < 3; ++m)
       LMOE_CK(h, lmoe::launch_absmax_groups(static_cast<cbf>(srcs[m]), static_cast<long long>(E),
-                                            mrows[m] * mcols[m], amax + m * E, h->sms, 0));
-    LMOE_CK(h, lmoe::launch_scales_from_amax(amax, static_cast<int>(3 * E), h->w_scale, 0));
+                                            mrows[m] * mcols[m], amax + m * E, h->sms, s));
+    LMOE_CK(h, lmoe::launch_scales_from_amax(amax, static_cast<int>(3 * E), h->w_scale, s));
     for (int m = 0; m < 3; ++m)
       LMOE_CK(h, lmoe::launch_quantize_e4m3(static_cast<cbf>(srcs[m]),
                                             static_cast<uint8_t*>(dsts[m]),
                                             static_cast<long long>(E) * mrows[m], mcols[m],
-                                            mrows[m], h->w_scale + m * E, true, h->sms, 0));
+                                            mrows[m], h->w_scale + m * E, true, h->sms, s));
   } else {
     for (int m = 0; m < 3; ++m)
       LMOE_CK(h, lmoe::launch_pack_tiles(srcs[m], dsts[m], static_cast<long long>(E) * mrows[m],
-                                         mcols[m] * 2, h->sms, 0));
+                                         mcols[m] * 2, h->sms, s));
   }
-  LMOE_CK(h, cudaDeviceSynchronize());
+  // the caller may free or reuse its buffers once this returns
+  LMOE_CK(h, cudaStreamSynchronize(s));
 
   bool ok = true;
   ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);

@@ -12,7 +12,9 @@
 // Host code may not pass the array's name to a kernel: on the host that name
 // is a stand-in, not a device address. The device address is looked up once
 // per device with cudaGetSymbolAddress, on the first call made while that
-// device is current, and cached.
+// device is current, and cached by device ordinal. The cache does not follow
+// a cudaDeviceReset (the module, and so the array, is then loaded again at
+// another address), which is why the header rules out calls after a reset.
 #include <mutex>
 
 #include "kernels.h"

@@ -107,7 +107,7 @@ int main(void) {
 
   latentmoe_t h = NULL;
   CHECK(latentmoe_create(&dims, k, 0, &h));
-  CHECK(latentmoe_load_weights(h, &w));
+  CHECK(latentmoe_load_weights(h, &w, NULL));
   CHECK(latentmoe_forward(h, x, y1, T, NULL));
   CHECK(latentmoe_forward(h, x, y2, T, NULL));
   uint32_t status = 1;

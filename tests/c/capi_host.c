@@ -44,7 +44,7 @@ int main(void) {
   expect(latentmoe_destroy(NULL) == LATENTMOE_OK, "destroy(NULL) is a no-op");
   expect(latentmoe_forward(NULL, NULL, NULL, 1, NULL) == LATENTMOE_ERR_INVALID_ARG,
          "forward(NULL)");
-  expect(latentmoe_load_weights(NULL, NULL) == LATENTMOE_ERR_INVALID_ARG, "load(NULL)");
+  expect(latentmoe_load_weights(NULL, NULL, NULL) == LATENTMOE_ERR_INVALID_ARG, "load(NULL)");
   expect(strcmp(latentmoe_strerror(LATENTMOE_ERR_TIMEOUT), "a bounded device wait timed out") == 0,
          "strerror(TIMEOUT)");
   expect(latentmoe_num_stages() == 10, "ten stages");

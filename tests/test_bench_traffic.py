@@ -36,3 +36,27 @@ def test_missing_summary_gives_no_traffic(monkeypatch, tmp_path):
     assert bench.profiled_traffic("mai-base-1") is None
     assert bench.profiled_traffic("tiny") is None
     assert os.path.isdir(tmp_path)
+
+
+def test_gate_up_algorithmic_bytes_are_the_touched_weights():
+    """The dominant kernel's algorithmic bytes count the gate and up weights of
+    the experts that got tokens only; z and h traffic is reported as built."""
+    from mixture_experts_layer_router_gb300 import synth
+    c = synth.CONFIGS["mai-base-1"]
+    flops, algo, built = bench.gate_up_work(c, 512)
+    assert algo == 512 * 2 * 10240 * 3072 * 2  # 64.42 GB
+    assert built == algo + c.T * c.k * (3072 + 10240) * 2
+    assert flops == 2 * c.T * c.k * 3072 * 2 * 10240
+    _, algo8, _ = bench.gate_up_work(c, 300, eb=1)
+    assert algo8 == 300 * 2 * 10240 * 3072
+
+
+def test_layer_roofline_peak_follows_the_power_cap():
+    from mixture_experts_layer_router_gb300 import synth
+    c = synth.CONFIGS["mid"]
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    a = bench.layer_roofline(c, 64, 1.0, peaks, "measured", False, False, capped=False)
+    b = bench.layer_roofline(c, 64, 1.0, peaks, "measured", False, False, capped=True)
+    assert a["flops"] == c.T * bench.layer_flops_per_token(c)
+    assert abs(a["tc_ms"] * 1900.0 - b["tc_ms"] * 1700.0) < 1e-9 * a["tc_ms"] * 1900.0
+    assert a["frac"] == max(a["tc_ms"], a["hbm_ms"]) and "burst" in a["tensor_peak"]

@@ -1,13 +1,15 @@
 """The multi-round fixed-capacity expert schedule on the GPU: the schedule
-bit for bit against the oracle's, and the layer output bitwise equal to the
-one-pass forward (no slot is dropped; every slot's expert rows are computed
-by the same kernels with the same arithmetic)."""
+bit for bit against the oracle's, the layer output against the oracle's
+layer routed from the GPU logits, and bitwise equal to the one-pass forward
+(no slot is dropped; every slot's expert rows are computed by the same
+kernels with the same arithmetic)."""
 import numpy as np
 import pytest
 import torch
 
 from mixture_experts_layer_router_gb300 import capi, synth
 import gpu_helpers as gh
+from oracle import latentmoe_ref as ref
 from oracle import multiround as mr
 
 pytestmark = pytest.mark.gpu
@@ -18,6 +20,21 @@ def _layer(name, seed=0, fp8=False):
     w = synth.make_weights(cfg, seed, "cuda")
     x = synth.make_x(cfg, seed, "cuda")
     return cfg, w, x, gh.make_layer(cfg, w, fp8=fp8)
+
+
+_ORACLE_Y = {}
+
+
+def _oracle_y(name, seed, w, x, logits):
+    """The oracle's layer output routed from the GPU logits, once per workload."""
+    key = (name, seed)
+    if key not in _ORACLE_Y:
+        cfg = synth.CONFIGS[name]
+        _ORACLE_Y[key] = (logits.clone(), ref.forward(gh.f64(x), gh.oracle_weights(w), cfg.k,
+                                                      logits=gh.f64(logits))["y"])
+    L0, y = _ORACLE_Y[key]
+    assert torch.equal(L0, logits)  # the same routing as the cached oracle run
+    return y
 
 
 def _forward(layer, x, fp8):
@@ -46,6 +63,8 @@ def test_schedule_matches_oracle_and_output_matches_one_pass(name, C, G):
     assert np.array_equal(take[:want["R"]], want["take"])
     assert not take[want["R"]:].any()
     assert torch.equal(y0, y1)
+    L1 = layer.get_routing(cfg.T, "cuda")["logits"]
+    gh.assert_y_close(y1, _oracle_y(name, 1, w, x, L1), what=f"{name} C={C} G={G}")
 
 
 @pytest.mark.parametrize("pairs", [True, False])

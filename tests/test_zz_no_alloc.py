@@ -1,4 +1,5 @@
-"""The allocation-free routing entry point against the regular one (GPU).
+"""The allocation-free routing entry point against the oracle and the
+regular entry point (GPU).
 
 latentmoe_route_from_logits_static serves callers that cannot allocate
 device memory (an application whose own pool owns the whole device, or a
@@ -15,6 +16,7 @@ import torch
 
 from mixture_experts_layer_router_gb300 import capi
 import gpu_helpers as gh
+from oracle import latentmoe_ref as ref
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +51,7 @@ def _static_route(L, k, renorm):
 
 @pytest.mark.parametrize("T,E,k,renorm", [(4096, 64, 4, False), (16384, 512, 8, False),
                                           (777, 100, 5, True)])
-def test_static_entry_matches_regular_entry_twice(T, E, k, renorm):
+def test_static_entry_matches_oracle_and_regular_entry_twice(T, E, k, renorm):
     gh.lib()
     layer = capi.LatentMoE(128, 128, E, k, 128, 0, max_tokens=T, renorm=renorm)
     for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs
@@ -61,7 +63,31 @@ def test_static_entry_matches_regular_entry_twice(T, E, k, renorm):
             assert torch.equal(got[key], want[key]), (call, key)
         np.testing.assert_allclose(got["gates"].cpu().numpy(), want["gates"].cpu().numpy(),
                                    rtol=2e-6, atol=1e-9)
+        # and against the oracle's routing of the same logits
+        gh.assert_routing_equal(got, ref.route(gh.f64(L), E, k, renorm=renorm), T, k)
     layer.close()
+
+
+def test_static_entry_allocates_nothing():
+    """After the first call on the device (which loads the library's module
+    and looks up the array's address), further calls leave the device's free
+    memory exactly as it was."""
+    T, E, k = 16384, 512, 8
+    L = _logits(T, E, 7)
+    _static_route(L, k, False)  # first call on this device: set-up
+    outs = _static_route(L, k, False)  # outputs allocated before the measurement
+    lib = gh.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    ptrs = [outs[n].data_ptr() for n in ("idx", "gates", "counts", "offsets", "perm", "pos")]
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert lib.latentmoe_route_from_logits_static(L.data_ptr(), T, E, k, 0, *ptrs, s) == \
+            capi.OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    gh.assert_routing_equal(outs, ref.route(gh.f64(L), E, k), T, k)
 
 
 def test_static_entry_rejects_sizes_beyond_its_scratch():
