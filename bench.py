@@ -360,6 +360,8 @@ def measure_small(cfg, args, peaks, peak_src, local, cpu_tokens):
     layer = capi.LatentMoE(cfg.d, cfg.l, cfg.E, cfg.k, cfg.F, cfg.Fs, max_tokens=cfg.T,
                            router_bias=w["b_r"] is not None)
     layer.load_weights(w)
+    if args.no_pdl:
+        layer.set_pdl(False)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -448,6 +450,8 @@ def run_ours(args, cfg, rank, world, dist):
     layer.load_weights(w)
     if args.no_sm_pairs:
         layer.set_sm_pairs(False)
+    if args.no_pdl:
+        layer.set_pdl(False)
     if args.capacity > 0:
         layer.set_capacity(args.capacity, args.group_size, args.max_rounds)
     # the library holds its own (packed) copy; the expert weights the CPU
@@ -571,6 +575,8 @@ def run_ours(args, cfg, rank, world, dist):
         "config": workload_config(cfg),
         "variant": {"expert_gemm": "single-SM" if args.no_sm_pairs else
                     "SM pairs where shapes allow",
+                    "launch": "stream order" if args.no_pdl else
+                    "programmatic dependent launch",
                     **({"capacity": args.capacity, "group_size": args.group_size,
                         "rounds": rounds_info} if args.capacity > 0 else {})},
         "tflops": cfg.T * layer_flops_per_token(cfg) / (ms_step / 1e3) / 1e12,
@@ -622,6 +628,8 @@ def main():
                     help="FP8 E4M3 expert GEMMs with delayed scaling")
     ap.add_argument("--fp8-dense", action="store_true",
                     help="with --fp8: the latent projections and the shared expert in E4M3 too")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="the forward's kernels in plain stream order (comparison runs)")
     ap.add_argument("--no-sm-pairs", action="store_true",
                     help="expert GEMMs on single SMs instead of SM pairs (comparison runs)")
     ap.add_argument("--capacity", type=int, default=0,

@@ -108,8 +108,11 @@ enum {
 enum {
   LATENTMOE_STATUS_TIMEOUT = 1u,    /* a pipeline wait in a GEMM kernel gave up */
   LATENTMOE_STATUS_BAD_EXPERT = 2u, /* an expert id outside [0, E) reached the sort */
-  LATENTMOE_STATUS_ROUNDS = 4u      /* the capacity schedule needed more rounds than
+  LATENTMOE_STATUS_ROUNDS = 4u,     /* the capacity schedule needed more rounds than
                                        max_rounds; the slots left over were not computed */
+  LATENTMOE_STATUS_BOUNDS = 8u      /* bounds-checked debug build only: a store, scatter
+                                       write or combine read fell outside its buffer and
+                                       was skipped */
 };
 
 /* FP8 E4M3 GEMMs (LATENTMOE_FP8_EXPERTS, LATENTMOE_FP8_DENSE). "The Training and RL
@@ -377,6 +380,14 @@ int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info);
  *   tile.
  * Results are bitwise the same either way. Takes effect at the next forward. */
 int latentmoe_set_sm_pairs(latentmoe_t h, int enable);
+
+/* Programmatic dependent launch between the forward's kernels (enable = 1,
+ * the default) or plain stream order (0). With it, each kernel's CTAs may be
+ * scheduled while the kernel before it finishes and set up their shared
+ * memory and TMEM meanwhile; every kernel still waits for the one before it
+ * to complete before it reads that kernel's results, so the results are
+ * bitwise the same either way. Takes effect at the next forward. */
+int latentmoe_set_pdl(latentmoe_t h, int enable);
 
 /* Kernel launches issued by this handle since creation. */
 int latentmoe_get_launch_count(latentmoe_t h, int64_t* launches);

@@ -4,6 +4,12 @@ The translation units are compiled in parallel, then linked into
 ``mixture_experts_layer_router_gb300/_build/liblatentmoe.so`` with the CUDA
 runtime linked statically. A unit is rebuilt when it or any header is newer
 than its object file.
+
+``build(variant="bounds")`` builds the bounds-checked debug library
+``_build/bounds/liblatentmoe.so`` (compiled with -DLMOE_BOUNDS): every
+epilogue store, scatter write and combine read checks its row against its
+buffer, skips an access outside it and sets LATENTMOE_STATUS_BOUNDS. It is
+the stand-in for a memory checker; the regular library is unchanged by it.
 """
 from __future__ import annotations
 
@@ -49,8 +55,15 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(nvcc: str, src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+VARIANTS = {None: [], "bounds": ["-DLMOE_BOUNDS"]}
+
+
+def lib_path(variant=None) -> str:
+    return LIB if variant is None else os.path.join(BUILD, variant, "liblatentmoe.so")
+
+
+def _compile(nvcc: str, src: str, extra, out_dir: str = BUILD) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src) + ".o")
     if _stale(obj, [src] + _headers()):
         cmd = [nvcc, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,23 +74,28 @@ def _compile(nvcc: str, src: str, extra) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    """Compile every unit and link the shared library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), variant=None) -> str:
+    """Compile every unit and link the shared library; returns its path.
+    variant: None (the library) or "bounds" (the bounds-checked debug build,
+    kept in its own folder)."""
+    out_dir = BUILD if variant is None else os.path.join(BUILD, variant)
+    lib = lib_path(variant)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
+    flags = list(VARIANTS[variant]) + list(extra_flags)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     workers = min(len(srcs), max(1, os.cpu_count() or 1))
     with ThreadPoolExecutor(max_workers=workers) as ex:
-        objs = list(ex.map(lambda s: _compile(nvcc, s, list(extra_flags)), srcs))
-    if _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB, *objs]
+        objs = list(ex.map(lambda s: _compile(nvcc, s, flags, out_dir), srcs))
+    if _stale(lib, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", lib, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose=True)
+    build(verbose=True, variant=sys.argv[1] if len(sys.argv) > 1 else None)

@@ -12,7 +12,9 @@ import os
 from typing import Dict, Optional  # noqa: F401
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "liblatentmoe.so")
+# LATENTMOE_LIB names another build of the same library (the bounds-checked
+# debug build, _build/bounds/liblatentmoe.so); there is no other fallback
+LIB_PATH = os.environ.get("LATENTMOE_LIB") or os.path.join(_PKG, "_build", "liblatentmoe.so")
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -34,6 +36,7 @@ FP8_TENSORS = 5  # scaled activations: z, h, x, c, shared hidden
 STATUS_TIMEOUT = 1
 STATUS_BAD_EXPERT = 2
 STATUS_ROUNDS = 4
+STATUS_BOUNDS = 8
 
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -72,6 +75,7 @@ SIGNATURES = {
     "latentmoe_num_stages": (ctypes.c_int, []),
     "latentmoe_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
     "latentmoe_get_launch_count": (ctypes.c_int, [_c_void_p, ctypes.POINTER(_i64)]),
+    "latentmoe_set_pdl": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
     "latentmoe_set_sm_pairs": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
     "latentmoe_set_capacity": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64]),
     "latentmoe_get_rounds": (ctypes.c_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_int32)]),
@@ -341,6 +345,10 @@ class LatentMoE:
     def set_sm_pairs(self, enable: bool) -> None:
         check(load().latentmoe_set_sm_pairs(self.handle, int(enable)),
               "latentmoe_set_sm_pairs")
+
+    def set_pdl(self, enable: bool) -> None:
+        check(load().latentmoe_set_pdl(self.handle, 1 if enable else 0), "latentmoe_set_pdl",
+              self.handle)
 
     def launch_count(self) -> int:
         v = _i64(0)

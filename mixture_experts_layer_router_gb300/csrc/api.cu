@@ -27,10 +27,14 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "kernels.h"
 #include "latentmoe.h"
@@ -190,7 +194,12 @@ struct latentmoe {
   __nv_bfloat16* cb = nullptr;
   __nv_bfloat16* sh = nullptr;
   unsigned* status = nullptr;
-  int* tile_counter = nullptr;  // SM-pair grouped kernels: dynamic tile scheduler
+  // {tile counter, exit count} of the SM-pair down GEMM, then the fused
+  // sort's {barrier arrivals, exits}: zero at create, and every launch leaves
+  // them zero (a wait that gave up may not: latentmoe_get_status clears them)
+  int* tile_counter = nullptr;
+  unsigned* sort_sync = nullptr;
+  bool pdl = true;              // programmatic dependent launch between the forward's kernels
   int64_t last_T = 0;
   // host-buffer forward staging
   void* x_stage = nullptr;
@@ -238,9 +247,42 @@ void record(latentmoe* h, int slot_base, int i, cudaStream_t s) {
   if (h->prof_slots > 0) cudaEventRecord(h->events[slot_base + i], s);
 }
 
+// NVTX ranges named after the forward's stages ("latentmoe:router", ...), so
+// that a profiler's timeline shows which stage enqueued which kernels. next(i)
+// closes the open range and opens stage i's (i = kNumStages opens none); the
+// destructor closes a range left open by an early error return. Without a
+// profiler attached the NVTX calls do nothing.
+class NvtxStages {
+ public:
+  void next(int i) {
+    if (open_) nvtxRangePop();
+    open_ = false;
+    if (i < kNumStages) {
+      char name[48];
+      snprintf(name, sizeof(name), "latentmoe:%s", kStageNames[i]);
+      nvtxRangePushA(name);
+      open_ = true;
+    }
+  }
+  ~NvtxStages() {
+    if (open_) nvtxRangePop();
+  }
+
+ private:
+  bool open_ = false;
+};
+
 // Counting sort of the workspace idx into counts, offsets, perm, pos.
 int run_sort(latentmoe* h, int T, cudaStream_t s) {
   const int E = static_cast<int>(h->dims.num_experts);
+  const int S = T * h->k;
+  if (lmoe::sort_fused_fits(S, E)) {
+    // one cooperative launch
+    LMOE_CK(h, lmoe::launch_sort_fused(h->idx, S, h->k, E, h->cnt, h->cbase, h->counts,
+                                       h->offsets, h->perm, h->pos, h->status, h->sort_sync, s));
+    h->launches += 1;
+    return LATENTMOE_OK;
+  }
   LMOE_CK(h, lmoe::launch_sort(h->idx, T * h->k, h->k, E, h->cnt, h->cbase, h->counts,
                                h->offsets, h->perm, h->pos, h->status, s));
   h->launches += lmoe::kSortLaunches;
@@ -276,6 +318,7 @@ int launch_expert_gate_up(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& 
   a.n_out = F;
   a.ldo = F;
   a.status = h->status;
+  if (a.out_rows == 0) a.out_rows = h->dims.max_tokens * h->k;
   if (h->fp8) {
     a.w_scale0 = h->w_scale;
     a.w_scale1 = h->w_scale + E;
@@ -306,6 +349,7 @@ int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok
   a.n_out = l;
   a.ldo = l;
   a.status = h->status;
+  if (a.out_rows == 0) a.out_rows = h->dims.max_tokens * h->k;
   a.w_scale0 = a.w_scale1 = a.in_scale = a.out_scale = nullptr;
   a.out_amax = nullptr;
   a.out_f32 = h->fp8_dense ? 1 : 0;
@@ -317,7 +361,6 @@ int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok
     a.fblocks = l / 512;
     // few long tiles per pair: dynamic tile order balances the last wave
     a.tile_counter = h->tile_counter;
-    LMOE_CK(h, cudaMemsetAsync(h->tile_counter, 0, sizeof(int), s));
     LMOE_CK(h, lmoe::launch_gemm_grouped_pair(lmoe::kGrpPlain, h->fp8, tok, h->m_wd, h->m_wd, a,
                                               h->sms, s));
   } else {
@@ -350,6 +393,7 @@ int run_expert_rounds(latentmoe* h, const CUtensorMap& mzp, cudaStream_t s) {
     a.in_start = h->rin + r * E;
     a.out_start = h->rout + r * (E + 1);
     a.out = h->hround;
+    a.out_rows = h->dims.num_experts * h->cap;
     int rc = launch_expert_gate_up(h, a, mzp, s);
     if (rc != LATENTMOE_OK) return rc;
     lmoe::GroupedArgs b;
@@ -480,10 +524,12 @@ int latentmoe_create(const latentmoe_dims* dims, int top_k, uint32_t flags, late
   h->sh = reinterpret_cast<__nv_bfloat16*>(base + o_sh);
   h->status = reinterpret_cast<unsigned*>(base + o_status);
   h->tile_counter = reinterpret_cast<int*>(base + o_tcount);
+  h->sort_sync = reinterpret_cast<unsigned*>(h->tile_counter + 2);
   h->f8 = reinterpret_cast<lmoe::Fp8State*>(base + o_f8);
   h->x8 = reinterpret_cast<uint8_t*>(base + o_x8);
   h->y32 = reinterpret_cast<float*>(base + o_y32);
   e = cudaMemset(h->status, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(h->tile_counter, 0, 16);
   if (e == cudaSuccess) {
     // delayed scaling starts with an empty history and unit scales
     lmoe::Fp8State init;
@@ -644,7 +690,8 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w,
   LMOE_CK(h, cudaStreamSynchronize(s));
 
   bool ok = true;
-  ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd, 256, lmoe::kRBK);
+  ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd,
+                 static_cast<uint32_t>(lmoe::router_w_box_rows(static_cast<int>(E))), lmoe::kRBK);
   if (h->fp8_dense)
     ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 128);
   else
@@ -689,6 +736,8 @@ namespace {
 int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_t s,
                  const int32_t* replay_idx, const float* replay_gates) {
   LMOE_CK(h, cudaSetDevice(h->device));
+  const lmoe::PdlScope pdl_scope(h->pdl);
+  NvtxStages nv;
   const latentmoe_dims& d = h->dims;
   const int E = static_cast<int>(d.num_experts), k = h->k;
   const int dd = static_cast<int>(d.hidden), l = static_cast<int>(d.latent);
@@ -719,6 +768,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
                             : 0;
   h->forwards += 1;
   record(h, slot_base, 0, s);
+  nv.next(0);
 
   // 0: router GEMM + softmax + stable top-k (fused); skipped when the caller
   // replays both choices and gates
@@ -740,6 +790,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 1, s);
+  nv.next(1);
   // 1: replayed choices (and gates from the router's softmax if not given)
   if (replay_idx != nullptr) {
     LMOE_CK(h, cudaMemcpyAsync(h->idx, replay_idx, static_cast<size_t>(S) * 4,
@@ -754,12 +805,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     }
   }
   record(h, slot_base, 2, s);
+  nv.next(2);
   // 2: counting sort
   {
     const int r = run_sort(h, Ti, s);
     if (r != LATENTMOE_OK) return r;
   }
   record(h, slot_base, 3, s);
+  nv.next(3);
   // 3: latent down-projection scattered to the expert-sorted slots (with
   // E4M3 dense GEMMs, x is quantized first)
   if (h->fp8_dense) {
@@ -778,6 +831,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.kb1 = dd / (h->fp8_dense ? lmoe::kBK8 : lmoe::kBK);
     a.out = h->zp;
     a.ldo = l;
+    a.out_rows = h->dims.max_tokens * h->k;
     a.pos = h->pos;
     a.topk = k;
     if (h->fp8) {
@@ -794,12 +848,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 4, s);
+  nv.next(4);
   if (h->cap > 0) {
     // 4+5: multi-round fixed-capacity schedule: per round, gate+up of the
     // round's slots into the fixed round buffer, then down back to the slots
     const int r = run_expert_rounds(h, mzp, s);
     if (r != LATENTMOE_OK) return r;
     record(h, slot_base, 5, s);
+    nv.next(5);
   } else {
     // 4: grouped gate+up with SwiGLU (weights on the M side, tokens on N)
     lmoe::GroupedArgs a;
@@ -809,22 +865,27 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     int r = launch_expert_gate_up(h, a, mzp, s);
     if (r != LATENTMOE_OK) return r;
     record(h, slot_base, 5, s);
+    nv.next(5);
     // 5: grouped expert down-projection
     a.out = h->ob;
     r = launch_expert_down(h, a, mh, s);
     if (r != LATENTMOE_OK) return r;
   }
   record(h, slot_base, 6, s);
+  nv.next(6);
   // 6: combine (E4M3 dense GEMMs: c written as codes)
   if (h->fp8_dense)
     LMOE_CK(h, lmoe::launch_combine_f8(reinterpret_cast<const float*>(h->ob), h->gates, h->pos,
                                        Ti, k, l,
                                        reinterpret_cast<uint8_t*>(h->cb), &h->f8->scale[3],
-                                       &h->f8->amax[3], s));
+                                       &h->f8->amax[3], h->dims.max_tokens * h->k, h->status,
+                                       s));
   else
-    LMOE_CK(h, lmoe::launch_combine(h->ob, h->gates, h->pos, Ti, k, l, h->cb, s));
+    LMOE_CK(h, lmoe::launch_combine(h->ob, h->gates, h->pos, Ti, k, l, h->cb,
+                                    h->dims.max_tokens * h->k, h->status, s));
   h->launches += 1;
   record(h, slot_base, 7, s);
+  nv.next(7);
   // 7: shared expert gate+up on the full width
   if (Fs > 0) {
     GemmMaps m = h->m_shared;
@@ -836,6 +897,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.kb1 = dd / (h->fp8_dense ? lmoe::kBK8 : lmoe::kBK);
     a.out = h->sh;
     a.ldo = Fs;
+    a.out_rows = h->dims.max_tokens;
     if (h->fp8_dense) {
       a.a_scale = &h->f8->scale[2];
       a.b_scale = &h->dw_scale[2];
@@ -848,6 +910,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 8, s);
+  nv.next(8);
   // 8: up-projection (+ shared expert's down-projection, K-concatenated; with
   // E4M3 dense GEMMs the two products have their own scales: the
   // up-projection leaves an fp32 partial that the shared down GEMM adds)
@@ -867,6 +930,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     if (Fs > 0) {
       a.out = h->y32;
       a.ldo = dd;
+      a.out_rows = h->dims.max_tokens;
       LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true, dense_pair_sms(h)));
       h->launches += 1;
       GemmMaps m2 = h->m_up;
@@ -881,6 +945,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
       b.ld_add = dd;
       b.out = out;
       b.ldo = dd;
+      b.out_rows = T;
       if (out32)
         LMOE_CK(h, lmoe::launch_gemm_f32(m2, b, grid, false, s, true, dense_pair_sms(h)));
       else
@@ -888,6 +953,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     } else {
       a.out = out;
       a.ldo = dd;
+      a.out_rows = T;
       if (out32)
         LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, false, s, true, dense_pair_sms(h)));
       else
@@ -906,6 +972,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     a.kb2 = Fs / lmoe::kBK;
     a.out = out;
     a.ldo = dd;
+    a.out_rows = T;
     const int grid = dense_grid(h, Ti, a.n_tiles);
     if (out32)
       LMOE_CK(h, lmoe::launch_gemm_f32(m, a, grid, Fs > 0, s, false, dense_pair_sms(h)));
@@ -914,12 +981,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     h->launches += 1;
   }
   record(h, slot_base, 9, s);
+  nv.next(9);
   // 9: delayed scaling: this forward's maxima enter the history, next scales
   if (h->fp8) {
     LMOE_CK(h, lmoe::launch_fp8_update(h->f8, kFp8Acts, s));
     h->launches += 1;
   }
   record(h, slot_base, 10, s);
+  nv.next(10);
   h->last_T = T;
   return LATENTMOE_OK;
 }
@@ -1042,6 +1111,8 @@ int latentmoe_get_status(latentmoe_t h, uint32_t* device_status) {
   unsigned v = 0;
   LMOE_CK(h, cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
   LMOE_CK(h, cudaMemset(h->status, 0, 4));
+  // a wait that gave up may have left the scheduling counters non-zero
+  if (v & LATENTMOE_STATUS_TIMEOUT) LMOE_CK(h, cudaMemset(h->tile_counter, 0, 16));
   *device_status = v;
   if (v & LATENTMOE_STATUS_TIMEOUT) return LATENTMOE_ERR_TIMEOUT;
   if (v != 0) return LATENTMOE_ERR_DEVICE_STATUS;
@@ -1157,6 +1228,12 @@ int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info) {
 int latentmoe_set_sm_pairs(latentmoe_t h, int enable) {
   if (h == nullptr || (enable != 0 && enable != 1)) return LATENTMOE_ERR_INVALID_ARG;
   h->sm_pairs = enable != 0;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_set_pdl(latentmoe_t h, int enable) {
+  if (h == nullptr || (enable != 0 && enable != 1)) return LATENTMOE_ERR_INVALID_ARG;
+  h->pdl = enable != 0;
   return LATENTMOE_OK;
 }
 
@@ -1335,12 +1412,13 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
     ga.n_out = static_cast<int>(N);
     ga.out = C;
     ga.ldo = N;
+    ga.out_rows = M;
     ga.status = status;
     cudaError_t e;
     if (pair) {
       ga.fblocks = static_cast<int>(mode == 2 ? N / 256 : N / 512);
       ga.tile_counter = reinterpret_cast<int*>(status) + 2;
-      e = cudaMemsetAsync(ga.tile_counter, 0, sizeof(int), s);
+      e = cudaMemsetAsync(ga.tile_counter, 0, 2 * sizeof(int), s);
       if (e == cudaSuccess)
         e = lmoe::launch_gemm_grouped_pair(mode == 2 ? lmoe::kGrpSwiglu : lmoe::kGrpPlain, false,
                                          tok, w0, w1, ga, num_sms(), s);
@@ -1378,6 +1456,7 @@ int debug_gemm_impl(const void* A, const void* B, void* C, const int32_t* offset
   a.group_m = 16;
   a.out = C;
   a.ldo = N;
+  a.out_rows = M;
   a.status = status;
   const long long tiles = static_cast<long long>(ceil_div(M, lmoe::kBM)) * a.n_tiles;
   const int grid = offsets ? num_sms() : static_cast<int>(tiles < num_sms() ? tiles : num_sms());
@@ -1453,6 +1532,7 @@ int latentmoe_debug_grouped_gemm_e4m3(const uint8_t* A, const uint8_t* B, const 
   ga.n_out = static_cast<int>(N);
   ga.out = C;
   ga.ldo = N;
+  ga.out_rows = M;
   ga.status = status;
   ga.in_scale = scales;
   ga.out_scale = scales + 1;

@@ -26,8 +26,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ o
                                                       const int* __restrict__ pos, int k, int l,
                                                       void* __restrict__ c,
                                                       const float* __restrict__ scale,
-                                                      unsigned* __restrict__ amax) {
+                                                      unsigned* __restrict__ amax,
+                                                      long long o_rows, unsigned* status) {
   __shared__ float red[4];
+  pdl_wait();
+  pdl_launch_dependents();
   const float inv = F8 ? inv_scale(*scale) : 1.0f;
   float m = 0.0f;
   __shared__ int sp[16];
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ o
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     for (int j = 0; j < k; ++j) {
       const int p = sp[j];
-      if (p < 0) continue;
+      if (p < 0 || !in_bounds(p, o_rows, status)) continue;
       const float g = sg[j];
       if constexpr (OF32) {
         const float4* src = reinterpret_cast<const float4*>(
@@ -92,15 +95,23 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ o
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* o, const float* gates, const int* pos, int T,
-                           int k, int l, __nv_bfloat16* c, cudaStream_t s) {
-  combine_kernel<false, false><<<T, 128, 0, s>>>(o, gates, pos, k, l, c, nullptr, nullptr);
+                           int k, int l, __nv_bfloat16* c, long long o_rows, unsigned* status,
+                           cudaStream_t s) {
+  const cudaError_t e = launch_kernel(combine_kernel<false, false>, dim3(T), dim3(128), 0, s, 1,
+                                      false, static_cast<const void*>(o), gates, pos, k, l,
+                                      static_cast<void*>(c), static_cast<const float*>(nullptr),
+                                      static_cast<unsigned*>(nullptr), o_rows, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_f8(const float* o, const float* gates, const int* pos, int T, int k,
                               int l, uint8_t* c, const float* scale, unsigned* amax,
-                              cudaStream_t s) {
-  combine_kernel<true, true><<<T, 128, 0, s>>>(o, gates, pos, k, l, c, scale, amax);
+                              long long o_rows, unsigned* status, cudaStream_t s) {
+  const cudaError_t e = launch_kernel(combine_kernel<true, true>, dim3(T), dim3(128), 0, s, 1,
+                                      false, static_cast<const void*>(o), gates, pos, k, l,
+                                      static_cast<void*>(c), scale, amax, o_rows, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -93,6 +93,7 @@ struct GemmArgs {
   int group_m;             // dense raster band, in m-tiles
   void* out;
   long long ldo;           // row stride of out, elements
+  long long out_rows;      // rows of the buffer out points to (bounds-checked build)
   const float* bias;       // kEpiF32, may be null
   const int* pos;          // kEpiScatter: [M * topk] destination rows (-1: skip)
   int topk;
@@ -184,11 +185,11 @@ __device__ __forceinline__ void store_chunk_bf16_staged(const GemmArgs& a,
       if constexpr (MODE == kEpiScatter) {
         for (int j = 0; j < a.topk; ++j) {
           const int dst_row = a.pos[row * a.topk + j];
-          if (dst_row < 0) continue;
+          if (dst_row < 0 || !in_bounds(dst_row, a.out_rows, a.status)) continue;
           *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
                                     static_cast<long long>(dst_row) * a.ldo + col + piece * 8) = w;
         }
-      } else {
+      } else if (in_bounds(row, a.out_rows, a.status)) {
         *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * a.ldo + col +
                                   piece * 8) = w;
       }
@@ -231,12 +232,13 @@ __device__ __forceinline__ void store_chunk_f8_scatter(const GemmArgs& a, const 
     if (rr < rows_valid) {
       const long long row = warp_row0 + rr;
       if (a.pos == nullptr) {
-        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + row * a.ldo + col + piece * 16) =
-            w;
+        if (in_bounds(row, a.out_rows, a.status))
+          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + row * a.ldo + col +
+                                    piece * 16) = w;
       } else {
         for (int j = 0; j < a.topk; ++j) {
           const int dst_row = a.pos[row * a.topk + j];
-          if (dst_row < 0) continue;
+          if (dst_row < 0 || !in_bounds(dst_row, a.out_rows, a.status)) continue;
           *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
                                     static_cast<long long>(dst_row) * a.ldo + col + piece * 16) = w;
         }
@@ -249,6 +251,7 @@ __device__ __forceinline__ void store_chunk_f8_scatter(const GemmArgs& a, const 
 template <int MODE>
 __device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&v)[32],
                                             long long row, int col) {
+  if (MODE != kEpiScatter && !in_bounds(row, a.out_rows, a.status)) return;
   if constexpr (MODE == kEpiF32) {
     float* dst = reinterpret_cast<float*>(a.out) + row * a.ldo + col;
     if (col + 32 <= a.N && (a.ldo & 3) == 0) {
@@ -286,7 +289,7 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&
     if constexpr (MODE == kEpiScatter) {
       for (int j = 0; j < a.topk; ++j) {
         const int dst_row = a.pos[row * a.topk + j];
-        if (dst_row < 0) continue;
+        if (dst_row < 0 || !in_bounds(dst_row, a.out_rows, a.status)) continue;
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
                                               static_cast<long long>(dst_row) * a.ldo + col);
         dst[0] = p[0]; dst[1] = p[1]; dst[2] = p[2]; dst[3] = p[3];
@@ -439,6 +442,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  // nothing above reads global memory: the set-up overlaps the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
   if (a.grouped) {
     for (int i = threadIdx.x; i <= a.num_groups; i += blockDim.x) seg_s[i] = a.seg_offsets[i];
   }

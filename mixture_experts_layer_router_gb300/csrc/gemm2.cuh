@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc_pair(tmem_slot, kTmemCols);
     tmem_relinquish_pair();
   }
+  // nothing above reads global memory: the set-up overlaps the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   // both CTAs' barriers are initialised before either touches the other's

@@ -19,8 +19,8 @@ static cudaError_t launch_grouped_impl(const CUtensorMap& tok, const CUtensorMap
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
   }
-  gemm_grouped_kernel<MODE, F8><<<grid, kGThreads, kGSmemBytes, s>>>(tok, w0, w1, a);
-  return cudaGetLastError();
+  return launch_kernel(gemm_grouped_kernel<MODE, F8>, dim3(grid), dim3(kGThreads), kGSmemBytes,
+                       s, 1, false, tok, w0, w1, a);
 }
 
 cudaError_t launch_gemm_grouped(int mode, bool f8, const CUtensorMap& tok, const CUtensorMap& w0,

@@ -84,10 +84,12 @@ struct GroupedArgs {
   void* out;               // bf16 [rows, n_out] (E4M3 SwiGLU: codes; plain with out_f32:
                            // fp32), rows in slot order
   long long ldo;
+  long long out_rows;      // rows of the buffer out points to (bounds-checked build)
   int out_f32;             // plain: fp32 output
   unsigned* status;
-  int* tile_counter;       // SM-pair kernel: [1] zero at launch; tiles past the first
-                           // wave are taken from it (null: static round robin)
+  int* tile_counter;       // SM-pair kernel: [2] {tile counter, exit count}, both zero at
+                           // launch and left zero by it; tiles past the first wave are
+                           // taken from [0] (null: static round robin)
   // E4M3 variant only
   const float* w_scale0;   // [G] scale of the weights of accumulator 0, per group
   const float* w_scale1;   // [G] accumulator 1 (SwiGLU: the up rows)
@@ -230,7 +232,7 @@ __device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_
   for (int q = 0; q < 4; ++q) {
     const int rr = q * 8 + (lane >> 2);
     const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * kGStagePitch + piece * 16);
-    if (rr < tok_valid)
+    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status))
       *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
                                 (tok_row0 + rr) * a.ldo + feat0 + piece * 8) = w;
   }
@@ -250,7 +252,8 @@ __device__ __forceinline__ void gstore_chunk_f32(const GroupedArgs& a, const uin
   float* out = static_cast<float*>(a.out) + feat0 + lane;
 #pragma unroll
   for (int j = 0; j < 32; ++j)
-    if (j < tok_valid) out[(tok_row0 + j) * a.ldo] = __uint_as_float(v[j]) * scale;
+    if (j < tok_valid && in_bounds(tok_row0 + j, a.out_rows, a.status))
+      out[(tok_row0 + j) * a.ldo] = __uint_as_float(v[j]) * scale;
 }
 
 __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint32_t (&q)[8],
@@ -269,7 +272,7 @@ __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint
     const int rr = h * 16 + (lane >> 1);
     const uint4 w =
         *reinterpret_cast<const uint4*>(stage + rr * 32 + ((piece ^ ((rr >> 2) & 1)) * 16));
-    if (rr < tok_valid)
+    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status))
       *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (tok_row0 + rr) * a.ldo + feat0 +
                                 piece * 16) = w;
   }
@@ -278,7 +281,8 @@ __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint
 
 // One tile's epilogue for one epilogue warp, shared by the single-SM and the
 // SM-pair kernels. The warp owns TMEM lanes [32 * quarter, +32) (lane_off)
-// and the 32-token chunks half, half + 2, ... of the tile's len tokens.
+// and the 32-token chunks half, half + 2, ... of the tile's len tokens
+// (len <= 256, or <= 512 for a plain tile with one accumulator).
 //   SwiGLU: h = SiLU(s_g acc0) * (s_u acc1) for output features
 //           [feat0, +32), written as bf16 or (F8) E4M3 codes with max |h| of the
 //           valid tokens folded into amax; TMEM is released before the stores.
@@ -421,6 +425,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  // nothing above reads global memory: the set-up overlaps the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
   load_group_table(a, gt);
   __syncthreads();
   if (warp == 2) build_tile_prefix(a, gt, a.fblocks);

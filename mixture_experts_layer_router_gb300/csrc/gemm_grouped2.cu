@@ -39,8 +39,8 @@ static cudaError_t launch_pair_impl(const CUtensorMap& tok, const CUtensorMap& w
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_clusters = n < sms / 2 ? n : sms / 2;
   }
-  cfg.gridDim = dim3(2 * max_clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, gemm_grouped_pair_kernel<MODE, F8>, tok, w0, w1, a);
+  return launch_kernel(gemm_grouped_pair_kernel<MODE, F8>, dim3(2 * max_clusters),
+                       dim3(kGThreads), kPSmemBytes, s, 2, false, tok, w0, w1, a);
 }
 
 cudaError_t launch_gemm_grouped_pair(int mode, bool f8, const CUtensorMap& tok,

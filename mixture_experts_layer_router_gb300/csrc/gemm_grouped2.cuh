@@ -14,7 +14,9 @@
 //           rows in accumulator 1) of pair tile p; its epilogue is the one-SM
 //           SwiGLU epilogue for those 128 features.
 //   plain:  accumulator a covers rows 512p + 256a .. +256 of W_d; CTA r holds
-//           rows 512p + 256a + 128r .. +128.
+//           rows 512p + 256a + 128r .. +128. An expert of more than 256 slots
+//           runs "wide" tiles instead (one accumulator of rows 256p + 128r ..
+//           +128 per CTA for up to 512 tokens; see wide_chunks below).
 //
 // Roles (both CTAs): warp 0 lane 0 loads its CTA's tiles (completing on the
 // leader's full barrier), warp 1 allocates TMEM (the leader's lane 0 also
@@ -25,7 +27,8 @@
 // Tile order: without GroupedArgs::tile_counter, every role walks the tiles
 // round robin itself (pair, pair + npairs, ...). With it, each pair's first
 // tile is its own index and the leader's producer takes the later ones from
-// that global counter (zeroed before the launch), so pairs whose tiles ran
+// that global counter (zero at launch; the last CTA to exit sets it back to
+// zero, so no memset sits between two launches), so pairs whose tiles ran
 // faster take more of them and the last wave ends together; the indices then
 // reach the other roles of both CTAs through a ring in shared memory
 // (tile_ring, tr_full, tr_empty). The down GEMM, with few long tiles per
@@ -58,16 +61,69 @@ struct PTile {
   int g;      // group
   int tok0;   // first token row of the chunk
   int out0;   // first output row of the chunk
-  int len;    // valid tokens (<= 256)
-  int n;      // MMA N: len rounded up to 16
-  int p;      // pair feature block
+  int len;    // valid tokens (<= 256; wide tiles <= 512)
+  int n;      // MMA N of the first MMA: len (wide: its first 256 tokens) rounded up to 16
+  int n2;     // wide tiles: MMA N of the second MMA (tokens 256.. of the chunk), else 0
+  int p;      // pair feature block (wide tiles: of 256 rows)
+  int wide;   // plain GEMM, expert of more than 256 slots: one accumulator, up to 512 tokens
 };
 
+// Plain (down) GEMM on SM pairs. An expert of n <= 256 slots takes fblocks
+// tiles of two accumulators (512 rows of W_d over the pair x its n tokens).
+// An expert of more slots takes ceil(n / 512) token chunks, split evenly, of
+// 2 * fblocks "wide" tiles: one accumulator (256 rows of W_d over the pair,
+// 128 per CTA) x all tokens of the chunk, in two MMAs whose results land at
+// TMEM columns [0, 256) and [256, 512), so that a token's column is its
+// index in the chunk. A wide tile moves one weight tile per k-block for up
+// to 512 tokens, where two chunk tiles of two accumulators would move the
+// weights twice for the same MACs.
+__device__ __forceinline__ void wide_chunks(int n, int& nch, int& cs) {
+  nch = (n + 2 * kGMaxTok - 1) / (2 * kGMaxTok);
+  const int per = (n + nch - 1) / nch;
+  cs = (per + 15) & ~15;
+}
+
+template <int MODE>
+__device__ __forceinline__ int pair_group_tiles(int n, int fblocks) {
+  if (n <= 0) return 0;
+  int nch, cs;
+  if (MODE == kGrpPlain && n > kGMaxTok) {
+    wide_chunks(n, nch, cs);
+    return nch * 2 * fblocks;
+  }
+  group_chunks(n, nch, cs);
+  return nch * fblocks;
+}
+
+// Exclusive prefix over groups of pair_group_tiles, by one warp.
+template <int MODE>
+__device__ __forceinline__ void build_pair_tile_prefix(const GroupedArgs& a, const GroupTable& gt) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  if (lane == 0) gt.tp[0] = 0;
+  for (int base = 0; base < a.num_groups; base += 32) {
+    const int g = base + lane;
+    int v = g < a.num_groups ? pair_group_tiles<MODE>(gt.len[g], a.fblocks) : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += o;
+    }
+    if (g < a.num_groups) gt.tp[g + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+template <int MODE>
 __device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const GroupTable& gt) {
   const int g = tile_group(t, a, gt);
   const int n = gt.len[g];
+  const bool wide = MODE == kGrpPlain && n > kGMaxTok;
   int nch, cs;
-  group_chunks(n, nch, cs);
+  if (wide)
+    wide_chunks(n, nch, cs);
+  else
+    group_chunks(n, nch, cs);
   const int local = t - gt.tp[g];
   const int p = local / nch;
   const int c = local - p * nch;
@@ -76,7 +132,14 @@ __device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const
   r.tok0 = gt.in[g] + c * cs;
   r.out0 = gt.out[g] + c * cs;
   r.len = min(cs, n - c * cs);
-  r.n = (r.len + 15) & ~15;
+  r.wide = wide ? 1 : 0;
+  if (wide) {
+    r.n = r.len >= kGMaxTok ? kGMaxTok : (r.len + 15) & ~15;
+    r.n2 = r.len > kGMaxTok ? (r.len - kGMaxTok + 15) & ~15 : 0;
+  } else {
+    r.n = (r.len + 15) & ~15;
+    r.n2 = 0;
+  }
   r.p = p;
   return r;
 }
@@ -138,9 +201,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tmem_alloc_pair(tmem_slot, 512);
     tmem_relinquish_pair();
   }
+  // nothing above reads global memory: the set-up overlaps the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
   load_group_table(a, gt);
   __syncthreads();
-  if (warp == 2) build_tile_prefix(a, gt, a.fblocks);
+  if (warp == 2) build_pair_tile_prefix<MODE>(a, gt);
   tc_fence_before_sync();
   __syncthreads();
   // both CTAs' barriers are initialised before either touches the other's
@@ -216,35 +282,55 @@ __global__ void __launch_bounds__(kGThreads, 1)
           t = read_tile(ring_slot, ring_ph);
         }
         if (t < 0) break;
-        const PTile c = decode_ptile(t, a, gt);
-        const int half = c.n >> 1;
+        const PTile c = decode_ptile<MODE>(t, a, gt);
+        // this CTA's token rows: half of the (first) MMA's N, and for a wide
+        // tile half of the second MMA's, from token 256 of the chunk on
+        const int half = c.n >> 1, half2 = c.n2 >> 1;
         const int nbox = (half + kGTokBox - 1) / kGTokBox;
-        const uint32_t bytes = 2u * (2 * kGWeightTile + nbox * kGTokBoxBytes);
+        const int nbox2 = (half2 + kGTokBox - 1) / kGTokBox;
+        const uint32_t bytes =
+            c.wide ? 2u * (kGWeightTile + (nbox + nbox2) * kGTokBoxBytes)
+                   : 2u * (2 * kGWeightTile + nbox * kGTokBoxBytes);
         int rt0, rt1;
         if (MODE == kGrpSwiglu) {
+          rt0 = rt1 = (c.g * a.w_group_rows) / 128 + 2 * c.p + static_cast<int>(rank);
+        } else if (c.wide) {
           rt0 = rt1 = (c.g * a.w_group_rows) / 128 + 2 * c.p + static_cast<int>(rank);
         } else {
           rt0 = (c.g * a.w_group_rows) / 128 + 4 * c.p + static_cast<int>(rank);
           rt1 = rt0 + 2;
         }
         const int tok_row = c.tok0 + static_cast<int>(rank) * half;
+        const int tok_row2 = c.tok0 + kGMaxTok + static_cast<int>(rank) * half2;
         for (int kb = 0; kb < a.kb; ++kb) {
           if (!wait_bounded_pair(&empty_bar[stage], phase ^ 1u, abort_flag, peer_abort,
                                  a.status)) {
             ok = false;
             break;
           }
+          // stage: [weights 0 | weights 1 | tokens], or for a wide tile
+          // [weights | tokens of the first MMA | tokens of the second]
           uint8_t* sw0 = tiles + stage * kPStageBytes;
           uint8_t* sw1 = sw0 + kGWeightTile;
           uint8_t* stok = sw1 + kGWeightTile;
           const uint32_t fb = mapa_shared(smem_addr(&full_bar[stage]), 0);
+          const int kc = kb * (F8 ? kGBK8 : kGBK);
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], bytes);
           tma_load_3d_pair(&tmW0, fb, sw0, 0, 0, rt0 * a.kb + kb, pol_w);
-          tma_load_3d_pair(MODE == kGrpSwiglu ? &tmW1 : &tmW0, fb, sw1, 0, 0, rt1 * a.kb + kb,
-                           pol_w);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d_pair(&tmTok, fb, stok + b * kGTokBoxBytes, kb * (F8 ? kGBK8 : kGBK),
-                             tok_row + b * kGTokBox, pol_t);
+          if (c.wide) {
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_pair(&tmTok, fb, sw1 + b * kGTokBoxBytes, kc, tok_row + b * kGTokBox,
+                               pol_t);
+            for (int b = 0; b < nbox2; ++b)
+              tma_load_2d_pair(&tmTok, fb, stok + b * kGTokBoxBytes, kc, tok_row2 + b * kGTokBox,
+                               pol_t);
+          } else {
+            tma_load_3d_pair(MODE == kGrpSwiglu ? &tmW1 : &tmW0, fb, sw1, 0, 0,
+                             rt1 * a.kb + kb, pol_w);
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_pair(&tmTok, fb, stok + b * kGTokBoxBytes, kc, tok_row + b * kGTokBox,
+                               pol_t);
+          }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kPStages) {
@@ -272,8 +358,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
       while (ok) {
         const int t = dynamic ? read_tile(ring_slot, ring_ph) : next_static(t_static);
         if (t < 0) break;
-        const PTile c = decode_ptile(t, a, gt);
+        const PTile c = decode_ptile<MODE>(t, a, gt);
         const uint32_t idesc = F8 ? instr_desc_e4m3(256, c.n) : instr_desc_bf16(256, c.n);
+        const uint32_t idesc2 =
+            F8 ? instr_desc_e4m3(256, c.n2 > 0 ? c.n2 : 16) : instr_desc_bf16(256, c.n2 > 0 ? c.n2 : 16);
         if (!wait_bounded_pair(tempty_bar, acc_phase ^ 1u, abort_flag, peer_abort, a.status))
           break;
         tc_fence_after_sync();
@@ -287,15 +375,33 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint64_t d0 = smem_desc_sw128(sw0);
           const uint64_t d1 = smem_desc_sw128(sw0 + kGWeightTile);
           const uint64_t dt = smem_desc_sw128(sw0 + 2 * kGWeightTile);
+          if (c.wide) {
+            // one weight tile; tokens [0, 256) into columns [0, 256), the
+            // rest of the chunk into columns [256, 512)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            if constexpr (F8) {
-              tc_mma_pair_f8(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
-              tc_mma_pair_f8(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
-            } else {
-              tc_mma_pair(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
-              tc_mma_pair(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              if constexpr (F8) {
+                tc_mma_pair_f8(tmem_base, d0 + 2ull * k, d1 + 2ull * k, idesc, accum);
+                if (c.n2 > 0)
+                  tc_mma_pair_f8(tmem_base + 256, d0 + 2ull * k, dt + 2ull * k, idesc2, accum);
+              } else {
+                tc_mma_pair(tmem_base, d0 + 2ull * k, d1 + 2ull * k, idesc, accum);
+                if (c.n2 > 0)
+                  tc_mma_pair(tmem_base + 256, d0 + 2ull * k, dt + 2ull * k, idesc2, accum);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              if constexpr (F8) {
+                tc_mma_pair_f8(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+                tc_mma_pair_f8(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+              } else {
+                tc_mma_pair(tmem_base, d0 + 2ull * k, dt + 2ull * k, idesc, accum);
+                tc_mma_pair(tmem_base + 256, d1 + 2ull * k, dt + 2ull * k, idesc, accum);
+              }
             }
           }
           tc_commit_pair(&empty_bar[stage], 0x3);
@@ -335,14 +441,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
         t = next_static(t_static);
       }
       if (t < 0) break;
-      const PTile c = decode_ptile(t, a, gt);
+      const PTile c = decode_ptile<MODE>(t, a, gt);
       if (!warp_wait_bounded_pair(tfull_bar, acc_phase, abort_flag, peer_abort, a.status)) break;
       tc_fence_after_sync();
       const int r = static_cast<int>(rank);
+      // a wide tile's one accumulator holds rows 256p + 128r .. of W_d for
+      // all len (<= 512) tokens, token j at column j
       const int feat0 = MODE == kGrpSwiglu ? (2 * c.p + r) * 128 + quarter * 32
+                        : c.wide           ? c.p * 256 + r * 128 + quarter * 32
                                            : c.p * 512 + r * 128 + quarter * 32;
       grouped_tile_epilogue<MODE, F8>(a, tmem_base + lane_off, half, c.g, c.len, c.out0, feat0,
-                                      feat0 + 256, true, in_s, out_inv, amax, stage_w, [&] {
+                                      feat0 + 256, !c.wide, in_s, out_inv, amax, stage_w, [&] {
                                         // one arrival per warp on the leader's barrier
                                         tc_fence_before_sync();
                                         __syncwarp();
@@ -365,6 +474,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, 512);
+  }
+  // the last CTA out sets the tile counter and the exit count back to zero
+  // (every producer has taken its last tile before its CTA gets here)
+  if (dynamic && threadIdx.x == 0) {
+    __threadfence();
+    unsigned* exits = reinterpret_cast<unsigned*>(a.tile_counter) + 1;
+    if (atomicAdd(exits, 1u) == gridDim.x - 1u) {
+      a.tile_counter[0] = 0;
+      *exits = 0u;
+      __threadfence();
+    }
   }
 }
 

@@ -47,9 +47,9 @@ static cudaError_t launch_gemm_pair_impl(const GemmMaps& m, const GemmArgs& a, i
   if (pairs > max_clusters) pairs = max_clusters;
   if (pairs > tiles) pairs = tiles;
   if (pairs < 1) pairs = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, DUAL, F8>, m.a, m.b, m.bu, m.a2,
-                            m.b2, a);
+  return launch_kernel(gemm_tc_pair_kernel<MODE, DUAL, F8>,
+                       dim3(static_cast<unsigned>(2 * pairs)), dim3(kGemmThreads),
+                       kPairGemmSmemBytes, s, 2, false, m.a, m.b, m.bu, m.a2, m.b2, a);
 }
 
 template <int MODE, bool DUAL, bool F8 = false>
@@ -66,9 +66,8 @@ static cudaError_t launch_gemm_impl(const GemmMaps& m, const GemmArgs& a, int gr
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
   }
-  gemm_tc_kernel<MODE, DUAL, F8><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(m.a, m.b, m.bu, m.a2,
-                                                                            m.b2, a);
-  return cudaGetLastError();
+  return launch_kernel(gemm_tc_kernel<MODE, DUAL, F8>, dim3(grid), dim3(kGemmThreads),
+                       kGemmSmemBytes, s, 1, false, m.a, m.b, m.bu, m.a2, m.b2, a);
 }
 
 }  // namespace lmoe

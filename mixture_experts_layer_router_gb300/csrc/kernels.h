@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <string.h>
 
 #include "gemm.cuh"
 #include "gemm_grouped.cuh"
@@ -19,6 +20,55 @@ inline int current_device_index() {
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
   return d;
+}
+
+// Programmatic dependent launch for the kernels this host thread enqueues
+// while a PdlScope with `on` is alive (the forward's launch sequence); every
+// kernel calls pdl_wait() before reading what earlier kernels wrote.
+inline bool& pdl_flag() {
+  thread_local bool on = false;
+  return on;
+}
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(bool on) : prev(pdl_flag()) { pdl_flag() = on; }
+  ~PdlScope() { pdl_flag() = prev; }
+};
+
+// One launch through cudaLaunchKernelEx: `cluster` CTAs per cluster (1: no
+// cluster), with the programmatic-serialization attribute when pdl_flag() is
+// set, and cooperative (every CTA resident at once) when `cooperative`.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, int cluster, bool cooperative, Args... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute at[3];
+  unsigned n = 0;
+  if (cluster > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_flag()) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cooperative) {
+    at[n].id = cudaLaunchAttributeCooperative;
+    at[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 struct GemmMaps {
@@ -95,7 +145,8 @@ struct Fp8State {
 cudaError_t launch_fp8_update(Fp8State* st, int n, cudaStream_t s);
 
 // Router GEMM fused with softmax and stable top-k: logits [T,E] fp32 (+bias),
-// idx [T,k], gates [T,k]; x map in 128-row boxes, W_r map in 256-row boxes.
+// idx [T,k], gates [T,k]; x map in 128-row boxes, W_r map in boxes of
+// router_w_box_rows(E) rows.
 cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,
                                cudaStream_t s);
 
@@ -124,6 +175,14 @@ inline long long sort_scratch_ints(long long S, long long E) {
 cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbase, int* counts,
                         int* offsets, int* perm, int* pos, unsigned* status, cudaStream_t s);
 constexpr int kSortLaunches = 3;
+// The same sort in one cooperative launch (kSortChunk slots per CTA, every
+// CTA resident at once): sort_fused_fits says whether the device holds the
+// ceil(S / kSortChunk) CTAs at once. sync: two counters, zero before the
+// first launch; every launch leaves them at zero again.
+bool sort_fused_fits(int S, int E);
+cudaError_t launch_sort_fused(const int* idx, int S, int k, int E, int* cnt, int* cbase,
+                              int* counts, int* offsets, int* perm, int* pos, unsigned* status,
+                              unsigned* sync, cudaStream_t s);
 
 // Multi-round fixed-capacity schedule (capacity C per expert per round,
 // groups of G consecutive experts, at most max_rounds rounds): per round r,
@@ -135,14 +194,16 @@ cudaError_t launch_round_schedule(const int* counts, const int* offsets, int E, 
                                   int max_rounds, int* rin, int* rout, int* rlen, int* info,
                                   unsigned* status, cudaStream_t s);
 
-// c[t] = sum_j gates[t,j] * o[pos[t,j]] in fp32, j order; bf16 out.
+// c[t] = sum_j gates[t,j] * o[pos[t,j]] in fp32, j order; bf16 out. o has
+// o_rows rows (checked in the bounds-checked build, which reports to status).
 cudaError_t launch_combine(const __nv_bfloat16* o, const float* gates, const int* pos, int T,
-                           int k, int l, __nv_bfloat16* c, cudaStream_t s);
+                           int k, int l, __nv_bfloat16* c, long long o_rows, unsigned* status,
+                           cudaStream_t s);
 // The same from fp32 o, with c written as E4M3 codes with *scale and max |c|
 // into *amax.
 cudaError_t launch_combine_f8(const float* o, const float* gates, const int* pos, int T, int k,
                               int l, uint8_t* c, const float* scale, unsigned* amax,
-                              cudaStream_t s);
+                              long long o_rows, unsigned* status, cudaStream_t s);
 // E4M3 codes of bf16 src [n] (n % 16 == 0) with *scale; max |src| into *amax.
 cudaError_t launch_quantize_act(const __nv_bfloat16* src, uint8_t* dst, long long n,
                                 const float* scale, unsigned* amax, int sms, cudaStream_t s);

@@ -17,6 +17,7 @@ namespace lmoe {
 constexpr unsigned kStatusTimeout = 1u;    // LATENTMOE_STATUS_TIMEOUT
 constexpr unsigned kStatusBadExpert = 2u;  // LATENTMOE_STATUS_BAD_EXPERT
 constexpr unsigned kStatusRounds = 4u;     // LATENTMOE_STATUS_ROUNDS
+constexpr unsigned kStatusBounds = 8u;     // LATENTMOE_STATUS_BOUNDS (bounds-checked build)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
 // Suspend-time hint of every try_wait: a waiting thread may sleep up to this
 // long (it wakes as soon as the phase completes) instead of returning to the
@@ -33,6 +34,23 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Bounds-checked debug build (compiled with -DLMOE_BOUNDS): every epilogue
+// store, scatter write and combine read asks in_bounds(i, n, status) whether
+// row i of a buffer of n rows exists; an access outside is skipped and sets
+// kStatusBounds in the device status word (nothing traps). In the regular
+// build in_bounds is the constant true and compiles away.
+#ifdef LMOE_BOUNDS
+__device__ __forceinline__ bool in_bounds(long long i, long long n, unsigned* status) {
+  if (i >= 0 && i < n) return true;
+  if (status != nullptr) atomicOr(status, kStatusBounds);
+  return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(long long, long long, unsigned*) {
+  return true;
+}
+#endif
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -111,6 +129,22 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// The forward's kernels are enqueued with programmatic stream serialization,
+// so a kernel's CTAs may be scheduled (and run their own shared-memory and
+// TMEM set-up) while the kernel before it is still finishing. Every kernel
+// therefore calls pdl_wait() before its first read of anything an earlier
+// kernel wrote: it returns once the preceding kernel has completed and its
+// writes are visible (at once for a kernel launched without the attribute).
+// Since every kernel waits before it completes, completion is transitive down
+// the chain. pdl_launch_dependents() then lets the next kernel be scheduled;
+// it is called after the wait, so at most one kernel runs ahead.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA

@@ -359,7 +359,8 @@ __global__ void __launch_bounds__(32) sort_scatter_kernel(const int* __restrict_
                                                           int E, const int* __restrict__ cbase,
                                                           const int* __restrict__ offsets,
                                                           int* __restrict__ perm,
-                                                          int* __restrict__ pos) {
+                                                          int* __restrict__ pos,
+                                                          unsigned* status) {
   extern __shared__ int run[];
   const int lane = threadIdx.x;
   for (int i = lane; i < E; i += 32)
@@ -383,8 +384,10 @@ __global__ void __launch_bounds__(32) sort_scatter_kernel(const int* __restrict_
     const int rank = __popc(peers & lt);
     if (valid) {
       const int slot = run[e] + rank;
-      perm[slot] = s / k;
-      pos[s] = slot;
+      if (in_bounds(slot, S, status)) {
+        perm[slot] = s / k;
+        pos[s] = slot;
+      }
     } else if (s < S) {
       pos[s] = -1;
     }
@@ -392,6 +395,208 @@ __global__ void __launch_bounds__(32) sort_scatter_kernel(const int* __restrict_
     if (valid && rank == 0) run[e] += __popc(peers);
     __syncwarp();
   }
+}
+
+// ---------------------------------------------------------------------------
+// The same counting sort in one cooperative launch (every CTA resident at
+// once). CTA b owns chunk b (kSortChunk slots); warp w of it owns the 128
+// slots [b * kSortChunk + 128 w, +128). Three phases, two grid barriers:
+//   1. per-warp expert histograms in shared memory; the CTA's sum is row b
+//      of cnt [chunks, E];
+//   2. expert e is scanned over the chunks by one warp of the grid (warp
+//      b * 8 + w takes experts e = b * 8 + w, + 8 * chunks, ...): cbase[b, e]
+//      is the exclusive prefix over chunks and counts[e] the total;
+//   3. every CTA forms offsets from counts (exclusive scan over experts; CTA 0
+//      writes them), turns its warp histograms into starting slots
+//      offsets[e] + cbase[b, e] + (slots of e in earlier warps of the chunk),
+//      and each warp ranks its slots in order, 32 at a time, exactly as
+//      sort_scatter_kernel does, so perm and pos are the three-kernel sort's.
+// The barrier counters (sync[0]: arrivals, sync[1]: exits) start at zero and
+// the last CTA to leave sets them back to zero for the next launch. A barrier
+// wait gives up after kWaitLimitNs and sets kStatusTimeout.
+constexpr int kFSortWarps = kSortChunk / 128;  // 8
+
+__device__ __forceinline__ bool grid_barrier(unsigned* arrivals, unsigned target,
+                                             unsigned* status, int* ok_smem) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(arrivals, 1u);
+    const uint64_t t0 = global_timer_ns();
+    int ok = 1;
+    while (*reinterpret_cast<volatile unsigned*>(arrivals) < target) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, kStatusTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *ok_smem = ok;
+  }
+  __syncthreads();
+  return *ok_smem != 0;
+}
+
+__global__ void __launch_bounds__(256) sort_fused_kernel(
+    const int* __restrict__ idx, int S, int k, int E, int* __restrict__ cnt,
+    int* __restrict__ cbase, int* __restrict__ counts, int* __restrict__ offsets,
+    int* __restrict__ perm, int* __restrict__ pos, unsigned* status, unsigned* sync) {
+  extern __shared__ int whist[];  // [kFSortWarps][E], later the warps' starting slots
+  __shared__ int ok_smem;
+  __shared__ int wtot[kFSortWarps];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = gridDim.x, b = blockIdx.x;
+  for (int i = threadIdx.x; i < kFSortWarps * E; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+
+  // 1. histograms: each distinct expert of a 32-slot step is added by its
+  // lowest lane (match_any), so a warp's row needs no atomics
+  const unsigned lt = (1u << lane) - 1u;
+  const int base = b * kSortChunk + warp * 128;
+  int ev[4];
+  bool bad = false;
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int sl = base + st * 32 + lane;
+    const int e = sl < S ? idx[sl] : -1;
+    ev[st] = e;
+    const bool valid = sl < S && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    if (sl < S && !valid) bad = true;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : (0x40000000 | lane));
+    if (valid && (peers & lt) == 0) whist[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) atomicOr(status, kStatusBadExpert);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kFSortWarps; ++w) c += whist[w * E + e];
+    cnt[static_cast<long long>(b) * E + e] = c;
+  }
+  if (!grid_barrier(&sync[0], static_cast<unsigned>(nb), status, &ok_smem)) return;
+
+  // 2. per-expert exclusive scan over the chunks, one warp per expert
+  for (int e = b * kFSortWarps + warp; e < E; e += nb * kFSortWarps) {
+    int carry = 0;
+    for (int c0 = 0; c0 < nb; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nb ? cnt[static_cast<long long>(c) * E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nb) cbase[static_cast<long long>(c) * E + e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) counts[e] = carry;
+  }
+  if (!grid_barrier(&sync[0], 2u * static_cast<unsigned>(nb), status, &ok_smem)) return;
+
+  // 3a. offsets: exclusive scan of counts over the experts (every CTA)
+  __shared__ int off_s[kMaxGroups + 1];
+  {
+    // thread i holds experts 2i, 2i + 1 (E <= 512)
+    const int e0 = 2 * threadIdx.x;
+    const int c0 = e0 < E ? counts[e0] : 0, c1 = e0 + 1 < E ? counts[e0 + 1] : 0;
+    int incl = c0 + c1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int wb = 0;
+    for (int w = 0; w < warp; ++w) wb += wtot[w];
+    const int ex = wb + incl - c0 - c1;
+    if (e0 < E) off_s[e0] = ex;
+    if (e0 + 1 < E) off_s[e0 + 1] = ex + c0;
+    if (e0 + 1 == E) off_s[E] = ex + c0;
+    if (e0 + 2 == E) off_s[E] = ex + c0 + c1;
+    __syncthreads();
+    if (b == 0)
+      for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off_s[e];
+  }
+  // 3b. starting slot of each expert for each warp of this chunk
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = off_s[e] + cbase[static_cast<long long>(b) * E + e];
+#pragma unroll
+    for (int w = 0; w < kFSortWarps; ++w) {
+      const int c = whist[w * E + e];
+      whist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3c. stable scatter of this warp's slots
+  int* run = whist + warp * E;
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int sl = base + st * 32 + lane;
+    const int e = ev[st];
+    const bool valid = sl < S && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : (0x40000000 | lane));
+    const int rank = __popc(peers & lt);
+    if (valid) {
+      const int slot = run[e] + rank;
+      if (in_bounds(slot, S, status)) {
+        perm[slot] = sl / k;
+        pos[sl] = slot;
+      }
+    } else if (sl < S) {
+      pos[sl] = -1;
+    }
+    __syncwarp();
+    if (valid && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+  }
+
+  // the last CTA out resets the barrier counters for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&sync[1], 1u) == static_cast<unsigned>(nb) - 1u) {
+      sync[0] = 0u;
+      sync[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+bool sort_fused_fits(int S, int E) {
+  static int max_blocks_of[kMaxDevices] = {};
+  const int dev = current_device_index();
+  if (dev < 0 || E > kMaxGroups) return false;
+  int& mb = max_blocks_of[dev];
+  if (mb == 0) {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, sort_fused_kernel, 256, static_cast<size_t>(kFSortWarps) * kMaxGroups * 4) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    mb = per_sm * sms;
+  }
+  const int nb = (S + kSortChunk - 1) / kSortChunk;
+  return nb <= mb;
+}
+
+cudaError_t launch_sort_fused(const int* idx, int S, int k, int E, int* cnt, int* cbase,
+                              int* counts, int* offsets, int* perm, int* pos, unsigned* status,
+                              unsigned* sync, cudaStream_t s) {
+  const int nb = (S + kSortChunk - 1) / kSortChunk;
+  const size_t smem = static_cast<size_t>(kFSortWarps) * E * sizeof(int);
+  return launch_kernel(sort_fused_kernel, dim3(nb), dim3(256), smem, s, 1, true, idx, S, k, E,
+                       cnt, cbase, counts, offsets, perm, pos, status, sync);
 }
 
 cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbase, int* counts,
@@ -404,7 +609,7 @@ cudaError_t launch_sort(const int* idx, int S, int k, int E, int* cnt, int* cbas
   sort_scan_kernel<<<1, 512, 0, s>>>(cnt, nb, E, cbase, counts, offsets);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sort_scatter_kernel<<<nb, 32, smem, s>>>(idx, S, k, E, cbase, offsets, perm, pos);
+  sort_scatter_kernel<<<nb, 32, smem, s>>>(idx, S, k, E, cbase, offsets, perm, pos, status);
   return cudaGetLastError();
 }
 

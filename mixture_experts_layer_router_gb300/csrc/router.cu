@@ -24,8 +24,8 @@ static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w
   }
   const int m_tiles = (a.T + 127) / 128;
   const int grid = m_tiles < sms ? m_tiles : sms;
-  router_topk_kernel<KMAX><<<grid, kRThreads, smem, s>>>(x, w, a);
-  return cudaGetLastError();
+  return launch_kernel(router_topk_kernel<KMAX>, dim3(grid), dim3(kRThreads), smem, s, 1, false,
+                       x, w, a);
 }
 
 cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,

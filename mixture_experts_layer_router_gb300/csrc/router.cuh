@@ -9,7 +9,8 @@
 // One CTA owns 128 token rows and all E <= 512 experts: L = x W_r^T (+ b)
 // accumulates in TMEM (128 lanes x E columns, fp32) from TMA-fed tcgen05 MMAs
 // (M = 128 tokens, N = up to 256 experts per instruction). The x map reads
-// 128 rows x 32 columns per box, the W_r map 256 rows x 32 columns.
+// 128 rows x 32 columns per box, the W_r map router_w_box_rows(E) rows x 32
+// columns.
 //
 // Epilogue: 16 warps, four per TMEM lane quarter (32 rows); the four warps
 // of a quarter split each row's experts.
@@ -62,8 +63,14 @@ struct RouterArgs {
   unsigned* status;
 };
 
+// Rows of the W_r box: the experts rounded up to 16 up to 256 experts (so a
+// small router moves no zero rows), else two boxes of 256 rows.
+__host__ __device__ constexpr int router_w_box_rows(int E) {
+  return E <= 256 ? ((E + 15) & ~15) : 256;
+}
+
 __host__ __device__ constexpr int router_stage_bytes(int E) {
-  return kRATile + ((E + 255) / 256) * kRBBox;
+  return kRATile + (E <= 256 ? router_w_box_rows(E) * kRBK * 2 : 2 * kRBBox);
 }
 
 template <int KMAX>
@@ -141,6 +148,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
+  // nothing above reads global memory: the set-up overlaps the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();

@@ -106,7 +106,7 @@ def test_worst_case_rounds_launch_count_and_errors():
     layer.forward(x)
     got = layer.rounds()
     assert got["launched"] == launched_want
-    assert layer.launch_count() - n0 == 9 + 1 + 2 * launched_want - 2
+    assert layer.launch_count() - n0 == 7 + 1 + 2 * launched_want - 2
     for bad in [(-1, 1, 0), (4, 0, 0), (4, cfg.E + 1, 0), (4, 2, -1)]:
         with pytest.raises(capi.LatentMoEError):
             layer.set_capacity(*bad)
