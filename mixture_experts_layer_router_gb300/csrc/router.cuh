@@ -17,7 +17,10 @@
 //   phase A: warp s of the quarter takes the 32-expert chunks c = s, s+4, ...:
 //            logits (+ bias) are stored for export, and each thread keeps its
 //            row's maximum and a ranked list of its largest logits (larger
-//            value first, lower expert id on equal values). The four partial
+//            value first, lower expert id on equal values): each group of 8
+//            logits is sorted by a fixed compare-and-swap network and merged
+//            into the list by a bitonic merge (short dependency chains; the
+//            same list as inserting the logits one by one). The four partial
 //            maxima and lists meet in shared memory.
 //   phase B: with the row maximum m, warp s forms partial sums
 //            p[i] = sum over c of exp(L[32c + i] - m) for i in [8s, 8s + 8),
@@ -101,6 +104,50 @@ __device__ __forceinline__ void topk_insert(float (&sv)[KMAX], int (&si)[KMAX], 
     sv[0] = x;
     si[0] = e;
   }
+}
+
+// Compare-and-swap in ranking order: afterwards (va, ia) ranks before (vb, ib).
+__device__ __forceinline__ void rank_cswap(float& va, int& ia, float& vb, int& ib) {
+  const bool sw = ranks_before(vb, ib, va, ia);
+  const float tv = sw ? vb : va;
+  const int ti = sw ? ib : ia;
+  vb = sw ? va : vb;
+  ib = sw ? ia : ib;
+  va = tv;
+  ia = ti;
+}
+
+// Sorts 8 (value, expert) pairs into ranking order with a fixed network of 19
+// compare-and-swaps in 6 layers (it sorts every 0-1 input, hence every input).
+__device__ __forceinline__ void rank_sort8(float (&v)[8], int (&i)[8]) {
+  constexpr int kNet[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                               {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                               {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) rank_cswap(v[kNet[c][0]], i[kNet[c][0]], v[kNet[c][1]], i[kNet[c][1]]);
+}
+
+// The first K of two lists in ranking order (sv/si of K, gv/gi of at least
+// K), into sv/si, in ranking order: element j of the list against element
+// K-1-j of the other keeps the better, which leaves a bitonic sequence
+// holding the best K; log2(K) half-cleaning layers sort it. Equal to
+// inserting the other list's elements one by one, for any K in {2, 4, 8}.
+template <int K, int N>
+__device__ __forceinline__ void rank_merge(float (&sv)[K], int (&si)[K], const float (&gv)[N],
+                                           const int (&gi)[N]) {
+  static_assert(K <= N && (K & (K - 1)) == 0, "merge of a power-of-two list");
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    if (ranks_before(gv[K - 1 - j], gi[K - 1 - j], sv[j], si[j])) {
+      sv[j] = gv[K - 1 - j];
+      si[j] = gi[K - 1 - j];
+    }
+  }
+#pragma unroll
+  for (int st = K / 2; st >= 1; st >>= 1)
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+      if ((j & st) == 0) rank_cswap(sv[j], si[j], sv[j + st], si[j + st]);
 }
 
 template <int KMAX>
@@ -268,35 +315,43 @@ __global__ void __launch_bounds__(kRThreads, 1)
           uint32_t v[8];
           tmem_ld_8cols(lane_base + e0, v);
           tmem_ld_wait();
+          float xv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float x = __uint_as_float(v[i]);
             if (e0 + i < a.E && a.bias != nullptr && !a.bias_select) x += a.bias[e0 + i];
-            v[i] = __float_as_uint(x);
+            xv[i] = x;
           }
           if (row_ok) {
             if (e0 + 8 <= a.E && (a.E & 3) == 0) {
-              *reinterpret_cast<float4*>(lrow + e0) =
-                  make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
-                              __uint_as_float(v[2]), __uint_as_float(v[3]));
-              *reinterpret_cast<float4*>(lrow + e0 + 4) =
-                  make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]),
-                              __uint_as_float(v[6]), __uint_as_float(v[7]));
+              *reinterpret_cast<float4*>(lrow + e0) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+              *reinterpret_cast<float4*>(lrow + e0 + 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
             } else {
               for (int i = 0; i < 8; ++i)
-                if (e0 + i < a.E) lrow[e0 + i] = __uint_as_float(v[i]);
+                if (e0 + i < a.E) lrow[e0 + i] = xv[i];
             }
           }
+          // ranking keys (the logit, or logit + bias for a selection-only
+          // bias); columns past E get a key that never ranks
+          float gv[8];
+          int gi[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int e = e0 + i;
-            if (e >= a.E) break;
-            float x = __uint_as_float(v[i]);
-            x = (x != x) ? -INFINITY : x;
+            const bool in = e < a.E;
+            float x = xv[i];
+            x = (x != x || !in) ? -INFINITY : x;
             m = fmaxf(m, x);
-            // the ranking key: the logit, or logit + bias for a selection-only bias
-            const float xs = a.bias_select ? x + a.bias[e] : x;
-            topk_insert<KMAX>(sv, si, xs, e);
+            gv[i] = (in && a.bias_select) ? x + a.bias[e] : x;
+            gi[i] = in ? e : 0x7fffffff;
+          }
+          if constexpr (KMAX <= 8) {
+            // sort the 8 and merge them into the running list
+            rank_sort8(gv, gi);
+            rank_merge<KMAX, 8>(sv, si, gv, gi);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) topk_insert<KMAX>(sv, si, gv[i], gi[i]);
           }
         }
       }
@@ -314,18 +369,27 @@ __global__ void __launch_bounds__(kRThreads, 1)
       float p[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) p[j] = 0.0f;
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t v[8];
-        tmem_ld_8cols(lane_base + c * 32 + sub * 8, v);
+      for (int c0 = 0; c0 < nchunks; c0 += 2) {
+        // two chunks' 8 columns per TMEM wait; the sums still run over the
+        // chunks in ascending order
+        uint32_t v[2][8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (c0 + q < nchunks) tmem_ld_8cols(lane_base + (c0 + q) * 32 + sub * 8, v[q]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int e = c * 32 + sub * 8 + j;
-          if (e < a.E) {
-            float x = __uint_as_float(v[j]);
-            if (a.bias != nullptr && !a.bias_select) x += a.bias[e];
-            x = (x != x) ? -INFINITY : x;
-            p[j] += expf(x - m);
+        for (int q = 0; q < 2; ++q) {
+          const int c = c0 + q;
+          if (c >= nchunks) break;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = c * 32 + sub * 8 + j;
+            if (e < a.E) {
+              float x = __uint_as_float(v[q][j]);
+              if (a.bias != nullptr && !a.bias_select) x += a.bias[e];
+              x = (x != x) ? -INFINITY : x;
+              p[j] += expf(x - m);
+            }
           }
         }
       }
@@ -349,10 +413,22 @@ __global__ void __launch_bounds__(kRThreads, 1)
         // ranking order already
 #pragma unroll 1
         for (int s2 = 1; s2 < 4; ++s2) {
+          if constexpr (KMAX <= 8) {
+            float ov[KMAX];
+            int oi[KMAX];
 #pragma unroll
-          for (int j2 = 0; j2 < KMAX; ++j2) {
-            if (j2 >= k) break;
-            topk_insert<KMAX>(sv, si, xch->v[quarter][s2][j2][lane], xch->i[quarter][s2][j2][lane]);
+            for (int j2 = 0; j2 < KMAX; ++j2) {
+              ov[j2] = xch->v[quarter][s2][j2][lane];
+              oi[j2] = xch->i[quarter][s2][j2][lane];
+            }
+            rank_merge<KMAX, KMAX>(sv, si, ov, oi);
+          } else {
+#pragma unroll
+            for (int j2 = 0; j2 < KMAX; ++j2) {
+              if (j2 >= k) break;
+              topk_insert<KMAX>(sv, si, xch->v[quarter][s2][j2][lane],
+                                xch->i[quarter][s2][j2][lane]);
+            }
           }
         }
         float g[KMAX];
