@@ -330,22 +330,32 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
     }
   } else if constexpr (MODE == kGrpSwiglu) {
     // h for this warp's chunks (at most 4) packed to bf16 in registers, then
-    // TMEM goes back to the MMA before the slower transposing stores
+    // TMEM goes back to the MMA before the slower transposing stores. The
+    // chunks are read in 16-column halves, software-pipelined: the loads of
+    // half q + 1 are in flight while half q's SiLU * up is formed, so the
+    // TMEM reads and the arithmetic of the hold overlap.
     uint32_t hp[4][16];
+    uint32_t gv[2][16], uv[2][16];
+    tmem_ld_16cols(tmem_lanes + half * 32, gv[0]);
+    tmem_ld_16cols(tmem_lanes + 256 + half * 32, uv[0]);
+    tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = half + 2 * i;
-      if (ch < nchunks) {
-        uint32_t gv[32], uv[32];
-        tmem_ld_32cols(tmem_lanes + ch * 32, gv);
-        tmem_ld_32cols(tmem_lanes + 256 + ch * 32, uv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          hp[i][j] = pack_bf16x2(silu(__uint_as_float(gv[2 * j])) * __uint_as_float(uv[2 * j]),
-                                 silu(__uint_as_float(gv[2 * j + 1])) *
-                                     __uint_as_float(uv[2 * j + 1]));
+    for (int q = 0; q < 8; ++q) {
+      const int i = q >> 1, ch = half + 2 * i;
+      if (ch >= nchunks) break;
+      const int qn = q + 1, chn = half + 2 * (qn >> 1);
+      if (qn < 8 && chn < nchunks) {
+        const uint32_t col = chn * 32 + (qn & 1) * 16;
+        tmem_ld_16cols(tmem_lanes + col, gv[qn & 1]);
+        tmem_ld_16cols(tmem_lanes + 256 + col, uv[qn & 1]);
       }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        hp[i][(q & 1) * 8 + j] =
+            pack_bf16x2(silu(__uint_as_float(gv[q & 1][2 * j])) * __uint_as_float(uv[q & 1][2 * j]),
+                        silu(__uint_as_float(gv[q & 1][2 * j + 1])) *
+                            __uint_as_float(uv[q & 1][2 * j + 1]));
+      tmem_ld_wait();
     }
     release();
 #pragma unroll
