@@ -300,27 +300,35 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
   if constexpr (MODE == kGrpSwiglu && F8) {
     // gate scale with SiLU's halving folded in (exact)
     const float sg_half = 0.5f * (in_s * a.w_scale0[g]), su = in_s * a.w_scale1[g];
+    // the same 16-column software pipeline as the bf16 path below
     uint32_t hq[4][8];
+    uint32_t gv[2][16], uv[2][16];
+    tmem_ld_16cols(tmem_lanes + half * 32, gv[0]);
+    tmem_ld_16cols(tmem_lanes + 256 + half * 32, uv[0]);
+    tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = half + 2 * i;
-      if (ch < nchunks) {
-        uint32_t gv[32], uv[32];
-        tmem_ld_32cols(tmem_lanes + ch * 32, gv);
-        tmem_ld_32cols(tmem_lanes + 256 + ch * 32, uv);
-        tmem_ld_wait();
-        const int valid = len - ch * 32;
-        float hv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          hv[j] = silu_from_half(__uint_as_float(gv[j]) * sg_half) * (__uint_as_float(uv[j]) * su);
-          if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          hq[i][j] =
-              quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3], out_inv);
+    for (int q = 0; q < 8; ++q) {
+      const int i = q >> 1, ch = half + 2 * i;
+      if (ch >= nchunks) break;
+      const int qn = q + 1, chn = half + 2 * (qn >> 1);
+      if (qn < 8 && chn < nchunks) {
+        const uint32_t col = chn * 32 + (qn & 1) * 16;
+        tmem_ld_16cols(tmem_lanes + col, gv[qn & 1]);
+        tmem_ld_16cols(tmem_lanes + 256 + col, uv[qn & 1]);
       }
+      const int valid = len - ch * 32 - (q & 1) * 16;
+      float hv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        hv[j] = silu_from_half(__uint_as_float(gv[q & 1][j]) * sg_half) *
+                (__uint_as_float(uv[q & 1][j]) * su);
+        if (j < valid) amax = fmaxf(amax, fabsf(hv[j]));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        hq[i][(q & 1) * 4 + j] =
+            quant4_e4m3(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3], out_inv);
+      tmem_ld_wait();
     }
     release();
 #pragma unroll
