@@ -83,15 +83,29 @@ def assert_routing_equal(gpu: dict, ora: dict, T: int, k: int):
 # ---------------------------------------------------------------- token samples at full size
 
 def slot_chunks(n: int):
-    """[(first, end)) slot ranges, relative to an expert's first slot, of the
-    token chunks the expert GEMMs split an expert of n slots into: at most
-    256 slots per chunk, split evenly, each chunk a multiple of 16 slots
-    except the last."""
+    """[(first, end)) slot ranges, relative to an expert's first slot, of every
+    token chunk the expert GEMMs cut an expert of n slots into: the one-SM
+    kernels' and the SM-pair gate+up kernel's chunks (at most 256 slots,
+    split evenly, each a multiple of 16 slots except the last) and, for
+    n > 256, the SM-pair down GEMM's wide chunks (at most 512 slots, split
+    the same way) with the two token ranges of a wide chunk of more than 256
+    slots (its first 256 slots, which one MMA covers, and the rest, which a
+    second MMA covers)."""
     if n <= 0:
         return []
-    nch = -(-n // 256)
-    cs = (-(-n // nch) + 15) & ~15
-    return [(c * cs, min((c + 1) * cs, n)) for c in range(nch)]
+
+    def even(limit):
+        nch = -(-n // limit)
+        cs = (-(-n // nch) + 15) & ~15
+        return [(c * cs, min((c + 1) * cs, n)) for c in range(nch)]
+
+    out = even(256)
+    if n > 256:
+        for lo, hi in even(512):
+            out.append((lo, hi))
+            if hi - lo > 256:
+                out += [(lo, lo + 256), (lo + 256, hi)]
+    return sorted(set(out))
 
 
 def covering_tokens(routing: dict, T: int, k: int, n_min: int, seed: int = 1,

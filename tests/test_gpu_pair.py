@@ -25,7 +25,11 @@ def _offs(counts):
                         device="cuda")
 
 
-@pytest.mark.parametrize("counts", [[16], [1, 0, 300, 37], [256, 513, 0, 8, 130]])
+# 300, 513, 257, 512, 511, 1000 and 1537 slots: more than one token chunk in the
+# SwiGLU GEMM (even chunks of at most 256) and wide tiles in the down GEMM (one
+# accumulator over chunks of up to 512 tokens, the tokens past 256 in a second MMA)
+@pytest.mark.parametrize("counts", [[16], [1, 0, 300, 37], [256, 513, 0, 8, 130],
+                                    [257, 512, 1000], [1537, 3, 511]])
 @pytest.mark.parametrize("mode,N", [(2, 256), (2, 512), (0, 512), (0, 1024)])
 def test_pair_grouped_bf16_equals_single_sm(counts, mode, N):
     gh.lib()
@@ -61,10 +65,10 @@ def test_pair_grouped_bf16_equals_single_sm(counts, mode, N):
         o += n
 
 
+@pytest.mark.parametrize("counts", [[0, 37, 256, 300, 5, 130], [513, 257, 1000, 512]])
 @pytest.mark.parametrize("mode,N", [(1, 512), (2, 256)])
-def test_pair_grouped_e4m3_equals_single_sm(mode, N):
+def test_pair_grouped_e4m3_equals_single_sm(mode, N, counts):
     gh.lib()
-    counts = [0, 37, 256, 300, 5, 130]
     G, K = len(counts), 384
     M = sum(counts)
     A, _ = _int_codes((M, K), 31)
