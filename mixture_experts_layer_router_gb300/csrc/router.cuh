@@ -35,15 +35,18 @@
 
 namespace lmoe {
 
-// 32-column k-blocks (64-byte swizzle): at E = 512 a stage is 40 KB, so five
-// stages fit and the loads of several k-blocks are in flight at once.
+// 32-column k-blocks (64-byte swizzle): at E = 512 a stage is 40 KB and four
+// stages fit; at E = 64 a stage is 12 KB and fifteen fit. The ring takes all
+// the shared memory the exchange leaves: with one 128-token tile per CTA and
+// few CTAs (T = 4096: 32), the k-loop is bound by the DRAM latency of x, so
+// the bytes in flight per CTA set its speed.
 constexpr int kRBK = 32;
 constexpr int kRATile = 128 * kRBK * 2;   // 8 KB of x
 constexpr int kRBBox = 256 * kRBK * 2;    // 16 KB of W_r per 256 experts
-constexpr int kRMaxStages = 8;
+constexpr int kRMaxStages = 16;
 constexpr int kREpiWarps = 16;
 constexpr int kRThreads = 64 + 32 * kREpiWarps;  // producer, MMA, 16 epilogue warps
-constexpr int kRMaxSmem = 200 * 1024;
+constexpr int kRMaxSmem = 232448;                 // the most a CTA may have (227 KB)
 
 // Shared-memory exchange between the four warps of a lane quarter.
 template <int KMAX>
