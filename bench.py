@@ -362,6 +362,10 @@ def measure_small(cfg, args, peaks, peak_src, local, cpu_tokens):
     layer.load_weights(w)
     if args.no_pdl:
         layer.set_pdl(False)
+    if args.no_fusion:
+        layer.set_expert_fusion(0)
+    elif args.fusion:
+        layer.set_expert_fusion(1)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -452,6 +456,10 @@ def run_ours(args, cfg, rank, world, dist):
         layer.set_sm_pairs(False)
     if args.no_pdl:
         layer.set_pdl(False)
+    if args.no_fusion:
+        layer.set_expert_fusion(0)
+    elif args.fusion:
+        layer.set_expert_fusion(1)
     if args.capacity > 0:
         layer.set_capacity(args.capacity, args.group_size, args.max_rounds)
     # the library holds its own (packed) copy; the expert weights the CPU
@@ -577,6 +585,10 @@ def run_ours(args, cfg, rank, world, dist):
                     "SM pairs where shapes allow",
                     "launch": "stream order" if args.no_pdl else
                     "programmatic dependent launch",
+                    "expert_launches": "two (gate+up, down)" if args.no_fusion or
+                    args.no_sm_pairs or args.capacity > 0 else
+                    ("one fused launch where shapes allow" if args.fusion else
+                     "automatic: one fused launch for small layers, else two"),
                     **({"capacity": args.capacity, "group_size": args.group_size,
                         "rounds": rounds_info} if args.capacity > 0 else {})},
         "tflops": cfg.T * layer_flops_per_token(cfg) / (ms_step / 1e3) / 1e12,
@@ -630,6 +642,11 @@ def main():
                     help="with --fp8: the latent projections and the shared expert in E4M3 too")
     ap.add_argument("--no-pdl", action="store_true",
                     help="the forward's kernels in plain stream order (comparison runs)")
+    ap.add_argument("--no-fusion", action="store_true",
+                    help="run the two expert GEMMs as two launches")
+    ap.add_argument("--fusion", action="store_true",
+                    help="run the two expert GEMMs as one fused launch where the shapes allow "
+                         "(default: automatic, fused for small layers only)")
     ap.add_argument("--no-sm-pairs", action="store_true",
                     help="expert GEMMs on single SMs instead of SM pairs (comparison runs)")
     ap.add_argument("--capacity", type=int, default=0,

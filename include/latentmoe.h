@@ -381,6 +381,25 @@ int latentmoe_get_rounds(latentmoe_t h, int32_t* take, int32_t* info);
  * Results are bitwise the same either way. Takes effect at the next forward. */
 int latentmoe_set_sm_pairs(latentmoe_t h, int enable);
 
+/* Both expert GEMMs of the one-pass forward in one launch or in two: the
+ * per-expert SwiGLU FFNs of "The Training and RL Infrastructure Behind
+ * MAI-Thinking-1", section "The model the systems run" (MoE row),
+ * h = SiLU(z W_g^T) * (z W_u^T) then o = h W_d^T over each expert's slots.
+ * The fused launch interleaves the gate+up tiles and the down tiles of the
+ * SM-pair kernels in one persistent sequence: a down tile reads a feature
+ * block of h once every gate+up tile of that block of its expert has stored
+ * it, so the second GEMM fills the first one's tail.
+ * mode 0: two launches. mode 1: one launch wherever the shapes allow it (SM
+ * pairs, F % 256 == 0, l % 512 == 0, no capacity schedule). mode 2 (the
+ * default): one launch where the shapes allow it and the gate+up GEMM has at
+ * most 32 tiles per SM pair (the layer's expected tile count), two launches
+ * otherwise (large layers, where the tails weigh little).
+ * Results are bitwise the same in every mode. When the launch is fused, stage
+ * "expert_gate_up" of latentmoe_get_stage_times covers both GEMMs and
+ * "expert_down" is empty. Takes effect at the next forward. Errors:
+ * INVALID_ARG (h NULL, mode outside [0, 2]). */
+int latentmoe_set_expert_fusion(latentmoe_t h, int mode);
+
 /* Programmatic dependent launch between the forward's kernels (enable = 1,
  * the default) or plain stream order (0). With it, each kernel's CTAs may be
  * scheduled while the kernel before it finishes and set up their shared

@@ -28,7 +28,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liblatentmoe.so")
 
 SOURCES = ["api.cu", "route.cu", "combine.cu", "gemm_bf16.cu", "gemm_f32.cu",
-           "gemm_swiglu.cu", "gemm_scatter.cu", "gemm_scatter8.cu", "gemm_grouped.cu", "gemm_grouped2.cu",
+           "gemm_swiglu.cu", "gemm_scatter.cu", "gemm_scatter8.cu", "gemm_grouped.cu", "gemm_grouped2.cu", "gemm_fused.cu",
            "pack.cu",
            "router.cu", "route_static.cu", "fp8.cu", "multiround.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

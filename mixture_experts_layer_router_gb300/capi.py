@@ -77,6 +77,7 @@ SIGNATURES = {
     "latentmoe_get_launch_count": (ctypes.c_int, [_c_void_p, ctypes.POINTER(_i64)]),
     "latentmoe_set_pdl": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
     "latentmoe_set_sm_pairs": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
+    "latentmoe_set_expert_fusion": (ctypes.c_int, [_c_void_p, ctypes.c_int]),
     "latentmoe_set_capacity": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64]),
     "latentmoe_get_rounds": (ctypes.c_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     "latentmoe_last_cuda_error": (ctypes.c_int, [_c_void_p]),
@@ -345,6 +346,12 @@ class LatentMoE:
     def set_sm_pairs(self, enable: bool) -> None:
         check(load().latentmoe_set_sm_pairs(self.handle, int(enable)),
               "latentmoe_set_sm_pairs")
+
+    def set_expert_fusion(self, mode) -> None:
+        """0 (or False): two expert launches; 1 (or True): one fused launch where
+        the shapes allow; 2: automatic (the default)."""
+        check(load().latentmoe_set_expert_fusion(self.handle, int(mode)),
+              "latentmoe_set_expert_fusion", self.handle)
 
     def set_pdl(self, enable: bool) -> None:
         check(load().latentmoe_set_pdl(self.handle, 1 if enable else 0), "latentmoe_set_pdl",

@@ -215,9 +215,11 @@ __device__ __forceinline__ bool second_acc_used(const GroupedArgs& a, int f) {
 // tokens, bf16 pairs (token 2j, 2j+1) in p[j]) through the warp's staging rows
 // and store 64 contiguous bytes per token row. Tokens at or past `tok_valid`
 // are not stored.
+// HINT: the stores carry the L2 eviction policy pol.
+template <bool HINT = false>
 __device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_t (&p)[16],
                                              uint8_t* stage, long long tok_row0, int tok_valid,
-                                             int feat0) {
+                                             int feat0, uint64_t pol = 0) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -232,9 +234,14 @@ __device__ __forceinline__ void gstore_chunk(const GroupedArgs& a, const uint32_
   for (int q = 0; q < 4; ++q) {
     const int rr = q * 8 + (lane >> 2);
     const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * kGStagePitch + piece * 16);
-    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status))
-      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                (tok_row0 + rr) * a.ldo + feat0 + piece * 8) = w;
+    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status)) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                            (tok_row0 + rr) * a.ldo + feat0 + piece * 8);
+      if constexpr (HINT)
+        st_global_u4_hint(dst, w, pol);
+      else
+        *dst = w;
+    }
   }
   __syncwarp();
 }
@@ -256,9 +263,10 @@ __device__ __forceinline__ void gstore_chunk_f32(const GroupedArgs& a, const uin
       out[(tok_row0 + j) * a.ldo] = __uint_as_float(v[j]) * scale;
 }
 
+template <bool HINT = false>
 __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint32_t (&q)[8],
                                                 uint8_t* stage, long long tok_row0,
-                                                int tok_valid, int feat0) {
+                                                int tok_valid, int feat0, uint64_t pol = 0) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -272,9 +280,14 @@ __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint
     const int rr = h * 16 + (lane >> 1);
     const uint4 w =
         *reinterpret_cast<const uint4*>(stage + rr * 32 + ((piece ^ ((rr >> 2) & 1)) * 16));
-    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status))
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (tok_row0 + rr) * a.ldo + feat0 +
-                                piece * 16) = w;
+    if (rr < tok_valid && in_bounds(tok_row0 + rr, a.out_rows, a.status)) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                            (tok_row0 + rr) * a.ldo + feat0 + piece * 16);
+      if constexpr (HINT)
+        st_global_u4_hint(dst, w, pol);
+      else
+        *dst = w;
+    }
   }
   __syncwarp();
 }
@@ -289,13 +302,15 @@ __device__ __forceinline__ void gstore_chunk_f8(const GroupedArgs& a, const uint
 //   plain:  acc0 and acc1 (when `two`) scaled by s_w and written to features
 //           feat0 and feat1 (each only if below n_out), bf16 or fp32; TMEM is
 //           released after the stores.
-// release() hands TMEM back to the MMA issuer.
-template <int MODE, bool F8, typename Release>
+// release() hands TMEM back to the MMA issuer. HINT (SwiGLU): h is stored with
+// the L2 eviction policy store_pol.
+template <int MODE, bool F8, bool HINT = false, typename Release>
 __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint32_t tmem_lanes,
                                                       int half, int g, int len, long long out0,
                                                       int feat0, int feat1, bool two,
                                                       float in_s, float out_inv, float& amax,
-                                                      uint8_t* stage_w, Release release) {
+                                                      uint8_t* stage_w, Release release,
+                                                      uint64_t store_pol = 0) {
   const int nchunks = (len + 31) / 32;
   if constexpr (MODE == kGrpSwiglu && F8) {
     // gate scale with SiLU's halving folded in (exact)
@@ -334,7 +349,8 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = half + 2 * i;
-      if (ch < nchunks) gstore_chunk_f8(a, hq[i], stage_w, out0 + ch * 32, len - ch * 32, feat0);
+      if (ch < nchunks)
+        gstore_chunk_f8<HINT>(a, hq[i], stage_w, out0 + ch * 32, len - ch * 32, feat0, store_pol);
     }
   } else if constexpr (MODE == kGrpSwiglu) {
     // h for this warp's chunks (at most 4) packed to bf16 in registers, then
@@ -369,7 +385,8 @@ __device__ __forceinline__ void grouped_tile_epilogue(const GroupedArgs& a, uint
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = half + 2 * i;
-      if (ch < nchunks) gstore_chunk(a, hp[i], stage_w, out0 + ch * 32, len - ch * 32, feat0);
+      if (ch < nchunks)
+        gstore_chunk<HINT>(a, hp[i], stage_w, out0 + ch * 32, len - ch * 32, feat0, store_pol);
     }
   } else {
     const float so = F8 ? in_s * a.w_scale0[g] : 1.0f;

@@ -114,23 +114,23 @@ __device__ __forceinline__ void build_pair_tile_prefix(const GroupedArgs& a, con
   }
 }
 
+// Tile `local` of a group of n rows starting at input row in0 and output row
+// out0 (group index g), in the order of pair_group_tiles: feature block
+// major, then token chunk.
 template <int MODE>
-__device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const GroupTable& gt) {
-  const int g = tile_group(t, a, gt);
-  const int n = gt.len[g];
+__device__ __forceinline__ PTile ptile_of(int g, int local, int n, int in0, int out0) {
   const bool wide = MODE == kGrpPlain && n > kGMaxTok;
   int nch, cs;
   if (wide)
     wide_chunks(n, nch, cs);
   else
     group_chunks(n, nch, cs);
-  const int local = t - gt.tp[g];
   const int p = local / nch;
   const int c = local - p * nch;
   PTile r;
   r.g = g;
-  r.tok0 = gt.in[g] + c * cs;
-  r.out0 = gt.out[g] + c * cs;
+  r.tok0 = in0 + c * cs;
+  r.out0 = out0 + c * cs;
   r.len = min(cs, n - c * cs);
   r.wide = wide ? 1 : 0;
   if (wide) {
@@ -142,6 +142,12 @@ __device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const
   }
   r.p = p;
   return r;
+}
+
+template <int MODE>
+__device__ __forceinline__ PTile decode_ptile(int t, const GroupedArgs& a, const GroupTable& gt) {
+  const int g = tile_group(t, a, gt);
+  return ptile_of<MODE>(g, t - gt.tp[g], gt.len[g], gt.in[g], gt.out[g]);
 }
 
 // a.fblocks = pair feature blocks per group (SwiGLU F/256, plain l/512).

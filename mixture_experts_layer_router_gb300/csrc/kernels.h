@@ -108,6 +108,17 @@ cudaError_t launch_gemm_grouped_pair(int mode, bool f8, const CUtensorMap& tok,
                                      const CUtensorMap& w0, const CUtensorMap& w1,
                                      const GroupedArgs& a, int sms, cudaStream_t s);
 
+// Both expert GEMMs in one launch (gemm_fused.cuh): z, W_g, W_u (packed) ->
+// h -> W_d (packed) -> o, with a.gu and a.dn set as for the two pair launches
+// above (seg_offsets form only). Needs F % 256 == 0 and l % 512 == 0.
+// a.dep ([E * F / 256]) and a.tile_counter ([2]) are zero at launch and are
+// left zero. As many pairs as can be resident at once.
+struct FusedExpertArgs;
+cudaError_t launch_expert_fused(bool f8, const CUtensorMap& z, const CUtensorMap& wg,
+                                const CUtensorMap& wu, const CUtensorMap& h,
+                                const CUtensorMap& wd, const FusedExpertArgs& a, int sms,
+                                cudaStream_t s);
+
 // Rewrite a row-major matrix of `rows` rows of `row_bytes` bytes (rows % 128
 // == 0, row_bytes % 128 == 0) as contiguous tiles of 128 rows x 128 bytes,
 // tile index (row / 128) * (row_bytes / 128) + byte / 128: kGBK bf16 or

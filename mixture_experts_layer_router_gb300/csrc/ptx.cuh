@@ -192,6 +192,28 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// A 16-byte global store with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_global_u4_hint(uint4* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- cross-CTA completion counts
+// A 32-bit load with acquire semantics at GPU scope: writes released before
+// the value was stored (by any CTA) are visible after it.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's earlier global accesses (here: the acquire above)
+// before its later async-proxy accesses (TMA loads of what other CTAs wrote).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
