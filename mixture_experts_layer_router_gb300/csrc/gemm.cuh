@@ -302,6 +302,24 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& a, const uint32_t (&
   }
 }
 
+// Scatter epilogues: bring the destination rows of the warp's rows of a tile
+// (pos[row * topk ..], topk ints per row) into L1 before the epilogue waits
+// for the accumulator. The epilogue reads them for every 32-column chunk; with
+// them in L1 the first chunk's stores do not wait on a global load either,
+// which shows where a CTA's only tile ends the kernel (one wave of tiles).
+template <int MODE>
+__device__ __forceinline__ void prefetch_scatter_rows(const GemmArgs& a, long long warp_row0,
+                                                      int rows_valid) {
+  if constexpr (MODE == kEpiScatter || MODE == kEpiScatterF8) {
+    const int lane = threadIdx.x & 31;
+    if (lane < rows_valid) {
+      const int* p = a.pos + (warp_row0 + lane) * a.topk;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p + a.topk - 1));
+    }
+  }
+}
+
 // The epilogue of one tile for the calling warp: TMEM lanes [32 * quarter,
 // +32) of the accumulator at tbase hold rows row0 + 32 * quarter + lane of
 // the tile (rows valid rows from row0; fewer, or none, at the ragged end),
@@ -589,6 +607,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const TileCoord c = decode_tile(t, a, seg_s, mt_s, kBRowsPerTile);
+      prefetch_scatter_rows<MODE>(a, static_cast<long long>(c.row0) + quarter * 32,
+                                  c.rows - quarter * 32);
       if (!warp_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, a.status)) break;
       tc_fence_after_sync();
       const uint32_t tbase =

@@ -242,10 +242,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = pair; t < total_tiles; t += npairs) {
       int row0, n, brow;
       decode_pair_tile(t, a, kBRowsPerTile, row0, n, brow);
+      const int crow0 = row0 + static_cast<int>(rank) * kBM;
+      prefetch_scatter_rows<MODE>(a, static_cast<long long>(crow0) + quarter * 32,
+                                  min(kBM, a.M - crow0) - quarter * 32);
       if (!warp_wait_bounded_pair(&tfull_bar[acc], acc_phase, abort_flag, peer_abort, a.status))
         break;
       tc_fence_after_sync();
-      const int crow0 = row0 + static_cast<int>(rank) * kBM;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       dense_tile_epilogue<MODE, F8>(a, tbase, crow0, min(kBM, a.M - crow0), n, quarter, half,
