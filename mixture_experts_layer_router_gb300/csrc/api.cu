@@ -176,7 +176,7 @@ struct latentmoe {
   void* wmem = nullptr;          // one allocation holding every weight copy
   GemmMaps m_down, m_shared, m_up;  // dense GEMM maps (every box 128 rows)
   CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
-  CUtensorMap m_wr32;            // router weights in 32-column boxes (router kernel)
+  CUtensorMap m_wr;              // router weights in router_bk(E)-column boxes (router kernel)
   // workspace
   void* ws = nullptr;
   float* logits = nullptr;
@@ -759,8 +759,9 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w,
   LMOE_CK(h, cudaStreamSynchronize(s));
 
   bool ok = true;
-  ok &= make_map(&h->m_wr32, o.w_r, E, dd, dd,
-                 static_cast<uint32_t>(lmoe::router_w_box_rows(static_cast<int>(E))), lmoe::kRBK);
+  ok &= make_map(&h->m_wr, o.w_r, E, dd, dd,
+                 static_cast<uint32_t>(lmoe::router_w_box_rows(static_cast<int>(E))),
+                 static_cast<uint32_t>(lmoe::router_bk(static_cast<int>(E))));
   if (h->fp8_dense)
     ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 128);
   else
@@ -815,9 +816,10 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   const bool out32 = (h->flags & LATENTMOE_OUT_FP32) != 0;
 
   // activation maps for this call
-  CUtensorMap mx, mx32, mzp, mh, mc, msh;
+  CUtensorMap mx, mxr, mzp, mh, mc, msh;
   bool ok = make_map(&mx, x, T, dd, dd, 128);
-  ok &= make_map(&mx32, x, T, dd, dd, 128, lmoe::kRBK);
+  ok &= make_map(&mxr, x, T, dd, dd, 128,
+                 static_cast<uint32_t>(lmoe::router_bk(static_cast<int>(E))));
   ok &= make_token_map(&mzp, h->zp, S, l, h->fp8);
   ok &= make_token_map(&mh, h->hb, S, F, h->fp8);
   CUtensorMap mx8;
@@ -848,14 +850,14 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
     ra.E = E;
     ra.k = k;
     ra.renorm = (h->flags & LATENTMOE_RENORM) ? 1 : 0;
-    ra.kb = dd / lmoe::kRBK;
+    ra.kb = dd / lmoe::router_bk(static_cast<int>(E));
     ra.bias = (h->flags & (LATENTMOE_ROUTER_BIAS | LATENTMOE_SELECT_BIAS)) ? h->w.b_r : nullptr;
     ra.bias_select = (h->flags & LATENTMOE_SELECT_BIAS) ? 1 : 0;
     ra.logits = h->logits;
     ra.idx = h->idx;
     ra.gates = h->gates;
     ra.status = h->status;
-    LMOE_CK(h, lmoe::launch_router_topk(mx32, h->m_wr32, ra, h->sms, s));
+    LMOE_CK(h, lmoe::launch_router_topk(mxr, h->m_wr, ra, h->sms, s));
     h->launches += 1;
   }
   record(h, slot_base, 1, s);

@@ -4,7 +4,7 @@
 
 namespace lmoe {
 
-template <int KMAX>
+template <int KMAX, int BK>
 static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a,
                                       int sms, cudaStream_t s) {
   const int per_stage = router_stage_bytes(a.E);
@@ -18,22 +18,28 @@ static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w
   if (dev < 0) return cudaErrorInvalidDevice;
   if (!smem_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(
-        router_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRMaxSmem);
+        router_topk_kernel<KMAX, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRMaxSmem);
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
   }
   const int m_tiles = (a.T + 127) / 128;
   const int grid = m_tiles < sms ? m_tiles : sms;
-  return launch_kernel(router_topk_kernel<KMAX>, dim3(grid), dim3(kRThreads), smem, s, 1, false,
-                       x, w, a);
+  return launch_kernel(router_topk_kernel<KMAX, BK>, dim3(grid), dim3(kRThreads), smem, s, 1,
+                       false, x, w, a);
 }
 
 cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,
                                cudaStream_t s) {
-  if (a.k <= 2) return launch_router_impl<2>(x, w, a, sms, s);
-  if (a.k <= 4) return launch_router_impl<4>(x, w, a, sms, s);
-  if (a.k <= 8) return launch_router_impl<8>(x, w, a, sms, s);
-  return launch_router_impl<16>(x, w, a, sms, s);
+  if (router_bk(a.E) == 64) {
+    if (a.k <= 2) return launch_router_impl<2, 64>(x, w, a, sms, s);
+    if (a.k <= 4) return launch_router_impl<4, 64>(x, w, a, sms, s);
+    if (a.k <= 8) return launch_router_impl<8, 64>(x, w, a, sms, s);
+    return launch_router_impl<16, 64>(x, w, a, sms, s);
+  }
+  if (a.k <= 2) return launch_router_impl<2, 32>(x, w, a, sms, s);
+  if (a.k <= 4) return launch_router_impl<4, 32>(x, w, a, sms, s);
+  if (a.k <= 8) return launch_router_impl<8, 32>(x, w, a, sms, s);
+  return launch_router_impl<16, 32>(x, w, a, sms, s);
 }
 
 }  // namespace lmoe

@@ -35,14 +35,13 @@
 
 namespace lmoe {
 
-// 32-column k-blocks (64-byte swizzle): at E = 512 a stage is 40 KB and four
-// stages fit; at E = 64 a stage is 12 KB and fifteen fit. The ring takes all
-// the shared memory the exchange leaves: with one 128-token tile per CTA and
-// few CTAs (T = 4096: 32), the k-loop is bound by the DRAM latency of x, so
-// the bytes in flight per CTA set its speed.
+// k-blocks: 32 columns (64-byte swizzle) for E > 256, where a stage holds
+// 512 rows of W_r (40 KB; four stages fit), and 64 columns (128-byte swizzle)
+// for E <= 256: the TMA then reads 128-byte row pieces of x and W_r instead of
+// 64-byte ones, half the requests for the same bytes (at E = 64, 24 KB stages,
+// seven of them). The ring takes all the shared memory the exchange leaves.
 constexpr int kRBK = 32;
-constexpr int kRATile = 128 * kRBK * 2;   // 8 KB of x
-constexpr int kRBBox = 256 * kRBK * 2;    // 16 KB of W_r per 256 experts
+__host__ __device__ constexpr int router_bk(int E) { return E <= 256 ? 64 : 32; }
 constexpr int kRMaxStages = 16;
 constexpr int kREpiWarps = 16;
 constexpr int kRThreads = 64 + 32 * kREpiWarps;  // producer, MMA, 16 epilogue warps
@@ -59,7 +58,7 @@ struct RouterExchange {
 
 struct RouterArgs {
   int T, E, k, renorm;
-  int kb;                  // d / kRBK
+  int kb;                  // d / router_bk(E)
   int stages;              // shared-memory stages (set by the launcher)
   const float* bias;       // [E] or null
   int bias_select;         // 0: bias is part of the logits; 1: it only moves the top-k choice
@@ -75,8 +74,10 @@ __host__ __device__ constexpr int router_w_box_rows(int E) {
   return E <= 256 ? ((E + 15) & ~15) : 256;
 }
 
+// x tile (128 rows) plus the W_r boxes, for k-blocks of router_bk(E) columns
 __host__ __device__ constexpr int router_stage_bytes(int E) {
-  return kRATile + (E <= 256 ? router_w_box_rows(E) * kRBK * 2 : 2 * kRBBox);
+  return 128 * router_bk(E) * 2 +
+         (E <= 256 ? router_w_box_rows(E) * router_bk(E) * 2 : 2 * 256 * router_bk(E) * 2);
 }
 
 template <int KMAX>
@@ -153,13 +154,16 @@ __device__ __forceinline__ void rank_merge(float (&sv)[K], int (&si)[K], const f
       if ((j & st) == 0) rank_cswap(sv[j], si[j], sv[j + st], si[j + st]);
 }
 
-template <int KMAX>
+// BK = router_bk(E): the k-block width the tensor maps were made with.
+template <int KMAX, int BK>
 __global__ void __launch_bounds__(kRThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW, const RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kATile = 128 * BK * 2;  // x
+  constexpr int kBBox = 256 * BK * 2;   // W_r per 256 experts
   const int stage_bytes = router_stage_bytes(a.E);
   RouterExchange<KMAX>* xch = reinterpret_cast<RouterExchange<KMAX>*>(smem);
   uint8_t* tiles = smem + ((sizeof(RouterExchange<KMAX>) + 1023) & ~static_cast<size_t>(1023));
@@ -227,11 +231,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
             break;
           }
           uint8_t* sa = tiles + stage * stage_bytes;
-          uint8_t* sb = sa + kRATile;
+          uint8_t* sb = sa + kATile;
           mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          tma_load_2d(&tmX, &full_bar[stage], sa, kb * kRBK, t * 128, pol_x);
+          tma_load_2d(&tmX, &full_bar[stage], sa, kb * BK, t * 128, pol_x);
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(&tmW, &full_bar[stage], sb + b * kRBBox, kb * kRBK, b * 256, pol_w);
+            tma_load_2d(&tmW, &full_bar[stage], sb + b * kBBox, kb * BK, b * 256, pol_w);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == a.stages) {
@@ -263,11 +267,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
           tc_fence_after_sync();
           const uint8_t* sa = tiles + stage * stage_bytes;
-          const uint64_t da = smem_desc_sw64(sa);
-          const uint64_t db0 = smem_desc_sw64(sa + kRATile);
-          const uint64_t db1 = smem_desc_sw64(sa + kRATile + kRBBox);
+          const uint64_t da = BK == 64 ? smem_desc_sw128(sa) : smem_desc_sw64(sa);
+          const uint64_t db0 =
+              BK == 64 ? smem_desc_sw128(sa + kATile) : smem_desc_sw64(sa + kATile);
+          const uint64_t db1 = BK == 64 ? smem_desc_sw128(sa + kATile + kBBox)
+                                        : smem_desc_sw64(sa + kATile + kBBox);
 #pragma unroll
-          for (int k = 0; k < kRBK / 16; ++k) {
+          for (int k = 0; k < BK / 16; ++k) {
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
             tc_mma(tmem_base, da + 2ull * k, db0 + 2ull * k, id0, accum);
             if (n1 > 0) tc_mma(tmem_base + 256, da + 2ull * k, db1 + 2ull * k, id1, accum);
