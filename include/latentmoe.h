@@ -391,9 +391,9 @@ int latentmoe_set_sm_pairs(latentmoe_t h, int enable);
  * it, so the second GEMM fills the first one's tail.
  * mode 0: two launches. mode 1: one launch wherever the shapes allow it (SM
  * pairs, F % 256 == 0, l % 512 == 0, no capacity schedule). mode 2 (the
- * default): one launch where the shapes allow it and the gate+up GEMM has at
- * most 32 tiles per SM pair (the layer's expected tile count), two launches
- * otherwise (large layers, where the tails weigh little).
+ * default): one launch where the shapes allow it and the two GEMMs have at
+ * most 400 k-blocks of work per SM pair (expected from E, l, F and T k), two
+ * launches otherwise (large layers, where the tails weigh little).
  * Results are bitwise the same in every mode. When the launch is fused, stage
  * "expert_gate_up" of latentmoe_get_stage_times covers both GEMMs and
  * "expert_down" is empty. Takes effect at the next forward. Errors:

@@ -391,19 +391,24 @@ int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok
 }
 
 // Whether the one-pass forward of T tokens runs both expert GEMMs as one
-// launch. Automatic mode: when the gate+up GEMM has at most 32 pair tiles per
-// SM pair (expected E * F/256 * max(1, T k / (256 E)) tiles), the fused
-// launch takes the two launches' tails into one (measured 1-5% faster on the
-// expert GEMMs of T = 4096, E = 64, F = 2048); with hundreds of tiles per
-// pair (the MAI-Base shapes) the tails weigh little and the interleaved
-// order read 3% more from DRAM (1.5-4.5% slower), so the two launches run.
+// launch. Automatic mode: when each SM pair has at most 400 k-blocks of work
+// in the two GEMMs (expected from E, l, F and T k: E * F/256 * c gate+up
+// tiles of l/BK k-blocks and E * l/512 * c down tiles of F/BK, c = the token
+// chunks of an expert of T k / E slots), the second launch's tail is a large
+// part of the layer and the fused launch takes it in (measured 1-5% faster
+// on the expert GEMMs of T = 4096, E = 64, l = 1024, F = 2048: about 160
+// k-blocks per pair). With more work per pair (the MAI-Base shapes, and 1/16
+// of MAI-Base-1 at about 1200) the interleaved order read 3% more from DRAM
+// and measured 1.5-4.5% slower, so the two launches run.
 bool experts_fused(const latentmoe* h, int64_t T) {
   if (h->fuse_experts == 0 || !h->sm_pairs || h->dep == nullptr || h->cap > 0) return false;
   if (h->fuse_experts == 1) return true;
   const int64_t E = h->dims.num_experts, S = T * h->k;
+  const int64_t l = h->dims.latent, F = h->dims.ffn;
+  const int64_t bk = h->fp8 ? lmoe::kGBK8 : lmoe::kGBK;
   const int64_t chunks = S > 256 * E ? (S + 256 * E - 1) / (256 * E) : 1;
-  const int64_t tiles = E * (h->dims.ffn / 256) * chunks;
-  return tiles <= 32 * static_cast<int64_t>(h->sms / 2);
+  const int64_t kblocks = E * chunks * ((F / 256) * (l / bk) + (l / 512) * (F / bk));
+  return kblocks <= 400 * static_cast<int64_t>(h->sms / 2);
 }
 
 // Both expert GEMMs in one launch over the expert segments (h->offsets):
