@@ -283,6 +283,13 @@ class NvtxStages {
 int run_sort(latentmoe* h, int T, cudaStream_t s) {
   const int E = static_cast<int>(h->dims.num_experts);
   const int S = T * h->k;
+  if (S <= lmoe::kBlockSortMaxSlots) {
+    // one CTA
+    LMOE_CK(h, lmoe::launch_sort_block(h->idx, S, h->k, E, h->counts, h->offsets, h->perm,
+                                       h->pos, h->status, s));
+    h->launches += 1;
+    return LATENTMOE_OK;
+  }
   if (lmoe::sort_fused_fits(S, E)) {
     // one cooperative launch
     LMOE_CK(h, lmoe::launch_sort_fused(h->idx, S, h->k, E, h->cnt, h->cbase, h->counts,
@@ -311,9 +318,6 @@ int run_routing(latentmoe* h, const float* logits, int T, cudaStream_t s, int sl
   return LATENTMOE_OK;
 }
 
-// One launch of the grouped gate+up GEMM over the groups described in `a`
-// (segments and output set by the caller): weights, scales and the kernel
-// (SM pairs where F % 256 == 0) from the handle.
 // The arguments of the gate+up GEMM (one-SM form: fblocks = F / 128).
 void gate_up_args(latentmoe* h, lmoe::GroupedArgs& a) {
   const int E = static_cast<int>(h->dims.num_experts);
@@ -335,6 +339,9 @@ void gate_up_args(latentmoe* h, lmoe::GroupedArgs& a) {
   }
 }
 
+// One launch of the grouped gate+up GEMM over the groups described in `a`
+// (segments and output set by the caller): weights, scales and the kernel
+// (SM pairs where F % 256 == 0) from the handle.
 int launch_expert_gate_up(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok,
                           cudaStream_t s) {
   const int F = static_cast<int>(h->dims.ffn);
@@ -351,7 +358,6 @@ int launch_expert_gate_up(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& 
   return LATENTMOE_OK;
 }
 
-// The same for the grouped down GEMM (SM pairs where l % 512 == 0).
 // The arguments of the down GEMM (one-SM form: fblocks = ceil(l / 256)).
 void down_args(latentmoe* h, lmoe::GroupedArgs& a) {
   const int E = static_cast<int>(h->dims.num_experts);
@@ -373,6 +379,7 @@ void down_args(latentmoe* h, lmoe::GroupedArgs& a) {
   }
 }
 
+// The same for the grouped down GEMM (SM pairs where l % 512 == 0).
 int launch_expert_down(latentmoe* h, lmoe::GroupedArgs a, const CUtensorMap& tok, cudaStream_t s) {
   const int l = static_cast<int>(h->dims.latent);
   down_args(h, a);

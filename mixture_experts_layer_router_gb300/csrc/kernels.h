@@ -191,6 +191,12 @@ constexpr int kSortLaunches = 3;
 // ceil(S / kSortChunk) CTAs at once. sync: two counters, zero before the
 // first launch; every launch leaves them at zero again.
 bool sort_fused_fits(int S, int E);
+// The same sort in one CTA of 1024 threads (no grid barrier), for at most
+// kBlockSortMaxSlots slots and E <= kMaxGroups; counts, offsets, perm, pos as
+// above (cnt and cbase are not used).
+constexpr int kBlockSortMaxSlots = 4096;
+cudaError_t launch_sort_block(const int* idx, int S, int k, int E, int* counts, int* offsets,
+                              int* perm, int* pos, unsigned* status, cudaStream_t s);
 cudaError_t launch_sort_fused(const int* idx, int S, int k, int E, int* cnt, int* cbase,
                               int* counts, int* offsets, int* perm, int* pos, unsigned* status,
                               unsigned* sync, cudaStream_t s);

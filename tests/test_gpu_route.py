@@ -35,6 +35,8 @@ def _logits(T, E, seed, kind="normal"):
     (128, 16, 2, "normal"), (1000, 64, 4, "normal"), (4096, 64, 4, "skewed"),
     (777, 100, 5, "ties"), (64, 512, 8, "ties"), (33, 16, 16, "normal"),
     (256, 8, 3, "zeros"), (16384, 512, 8, "normal"), (8192, 256, 7, "normal"), (1, 4, 1, "normal"),
+    # around the one-CTA sort's limit (4096 slots): one CTA, then the cooperative launch
+    (1024, 512, 4, "skewed"), (4097, 64, 1, "ties"),
 ])
 def test_route_matches_oracle(T, E, k, kind):
     layer = _layer(E, k, T)
