@@ -20,9 +20,10 @@
 //   fence. Before a D tile's producers load h's k-blocks of a feature block,
 //   they wait (acquire, bounded) until that count reaches 16 x the expert's
 //   token chunks, then order the async-proxy loads after the acquire. h is
-//   stored with an evict-last policy, so that it is still in L2 when the D
-//   tiles read it a few hundred microseconds later; the two launches wrote
-//   it to DRAM and read it back.
+//   stored with an evict-last policy in the hope that the D tiles find it in
+//   L2; measured, they mostly do not (the launch reads what the two launches
+//   read from DRAM), so the gain is the second launch's tail, which matters
+//   only for small layers.
 //
 // Progress: every tile, the first of each pair included, is taken from the
 // global counter, so tiles are taken in sequence order and only by CTAs that
