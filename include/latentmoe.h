@@ -208,6 +208,28 @@ int latentmoe_forward_routed(latentmoe_t h, const void* x, const int32_t* idx,
 int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host,
                            int64_t T, latentmoe_stream_t stream);
 
+/* Pipelined form of latentmoe_forward_host for a stream of steps: enqueues
+ * the copy of x_host (bf16 [T, d]) to the device, the forward on `stream`,
+ * and the copy of the result to out_host, and returns without waiting. Two
+ * staging slots alternate between calls, with a copy stream for each
+ * direction, so the input copy of the next call and the output copy of the
+ * previous one run while this call's forward does. Every call still moves
+ * its own x in and its own result out. x_host must stay unchanged, and
+ * out_host unread, until latentmoe_host_wait has returned; host memory must
+ * be page-locked for the copies to overlap (pageable memory works but
+ * serialises). A call's forward follows the earlier forwards on `stream` as
+ * latentmoe_forward does; use one stream for the calls of a handle. Staging
+ * slots, streams and events are made on the first call and kept by the
+ * handle. Errors: as latentmoe_forward; a failed call leaves earlier calls'
+ * work enqueued. */
+int latentmoe_forward_host_async(latentmoe_t h, const void* x_host, void* out_host,
+                                 int64_t T, latentmoe_stream_t stream);
+
+/* Wait until every copy that latentmoe_forward_host_async enqueued (and so
+ * every forward they follow) has completed. Errors: INVALID_ARG (h NULL),
+ * CUDA. */
+int latentmoe_host_wait(latentmoe_t h);
+
 /* Free the workspace and the handle. NULL is accepted and ignored. */
 int latentmoe_destroy(latentmoe_t h);
 

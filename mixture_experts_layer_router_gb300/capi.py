@@ -62,6 +62,9 @@ SIGNATURES = {
     "latentmoe_forward_routed": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                                 _c_void_p, _i64, _c_void_p]),
     "latentmoe_forward_host": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
+    "latentmoe_forward_host_async": (ctypes.c_int, [_c_void_p, _c_void_p, _c_void_p, _i64,
+                                                    _c_void_p]),
+    "latentmoe_host_wait": (ctypes.c_int, [_c_void_p]),
     "latentmoe_destroy": (ctypes.c_int, [_c_void_p]),
     "latentmoe_route_from_logits": (ctypes.c_int, [_c_void_p, _c_void_p, _i64] + [_c_void_p] * 7),
     "latentmoe_route_from_logits_static": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_int,
@@ -214,6 +217,18 @@ class LatentMoE:
                                             x_host.shape[0], _stream(stream)),
               "latentmoe_forward_host")
         return out_host
+
+    def forward_host_async(self, x_host, out_host, stream=None):
+        """Pipelined host-buffer forward: returns at once; x_host must stay
+        unchanged and out_host unread until host_wait()."""
+        check(load().latentmoe_forward_host_async(self.handle, x_host.data_ptr(),
+                                                  out_host.data_ptr(), x_host.shape[0],
+                                                  _stream(stream)),
+              "latentmoe_forward_host_async")
+        return out_host
+
+    def host_wait(self) -> None:
+        check(load().latentmoe_host_wait(self.handle), "latentmoe_host_wait")
 
     def route_from_logits(self, logits, stream=None):
         import torch

@@ -211,6 +211,16 @@ struct latentmoe {
   // host-buffer forward staging
   void* x_stage = nullptr;
   void* y_stage = nullptr;
+  // pipelined host-buffer forward: two staging slots, a stream for the
+  // copies in and one for the copies out, and per slot the events that order
+  // them with the forwards (created on the first call)
+  void* xs[2] = {nullptr, nullptr};
+  void* ys[2] = {nullptr, nullptr};
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr};   // slot's x copied in
+  cudaEvent_t ev_fwd[2] = {nullptr, nullptr};  // slot's forward done (x read, y written)
+  cudaEvent_t ev_out[2] = {nullptr, nullptr};  // slot's y copied out
+  int64_t host_steps = 0;
   // profiling
   std::vector<cudaEvent_t> events;
   int prof_slots = 0;
@@ -632,6 +642,17 @@ int latentmoe_destroy(latentmoe_t h) {
   for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
   if (h->x_stage) cudaFree(h->x_stage);
   if (h->y_stage) cudaFree(h->y_stage);
+  if (h->copy_in) cudaStreamSynchronize(h->copy_in);
+  if (h->copy_out) cudaStreamSynchronize(h->copy_out);
+  for (int i = 0; i < 2; ++i) {
+    if (h->xs[i]) cudaFree(h->xs[i]);
+    if (h->ys[i]) cudaFree(h->ys[i]);
+    if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+    if (h->ev_fwd[i]) cudaEventDestroy(h->ev_fwd[i]);
+    if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+  }
+  if (h->copy_in) cudaStreamDestroy(h->copy_in);
+  if (h->copy_out) cudaStreamDestroy(h->copy_out);
   if (h->ws) cudaFree(h->ws);
   if (h->wmem) cudaFree(h->wmem);
   if (h->cap_mem) cudaFree(h->cap_mem);
@@ -1127,6 +1148,59 @@ int latentmoe_forward_host(latentmoe_t h, const void* x_host, void* out_host, in
   if (r != LATENTMOE_OK) return r;
   LMOE_CK(h, cudaMemcpyAsync(out_host, h->y_stage, y_bytes, cudaMemcpyDeviceToHost, s));
   LMOE_CK(h, cudaStreamSynchronize(s));
+  return LATENTMOE_OK;
+}
+
+int latentmoe_forward_host_async(latentmoe_t h, const void* x_host, void* out_host, int64_t T,
+                                 latentmoe_stream_t st) {
+  if (h == nullptr || x_host == nullptr || out_host == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->dims.max_tokens) return LATENTMOE_ERR_INVALID_ARG;
+  if (!h->loaded) return LATENTMOE_ERR_NOT_LOADED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(st);
+  LMOE_CK(h, cudaSetDevice(h->device));
+  const size_t x_bytes = static_cast<size_t>(T) * h->dims.hidden * 2;
+  const size_t y_bytes =
+      static_cast<size_t>(T) * h->dims.hidden * ((h->flags & LATENTMOE_OUT_FP32) ? 4 : 2);
+  if (h->copy_in == nullptr) {
+    // first call: staging slots, copy streams and events
+    const size_t xcap = static_cast<size_t>(h->dims.max_tokens) * h->dims.hidden * 2;
+    const size_t ycap = static_cast<size_t>(h->dims.max_tokens) * h->dims.hidden * 4;
+    for (int i = 0; i < 2; ++i) {
+      LMOE_CK(h, cudaMalloc(&h->xs[i], xcap));
+      LMOE_CK(h, cudaMalloc(&h->ys[i], ycap));
+      LMOE_CK(h, cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming));
+      LMOE_CK(h, cudaEventCreateWithFlags(&h->ev_fwd[i], cudaEventDisableTiming));
+      LMOE_CK(h, cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming));
+    }
+    LMOE_CK(h, cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking));
+    LMOE_CK(h, cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking));
+  }
+  const int slot = static_cast<int>(h->host_steps & 1);
+  // x in: once the forward two steps back has read this slot
+  if (h->host_steps >= 2) LMOE_CK(h, cudaStreamWaitEvent(h->copy_in, h->ev_fwd[slot], 0));
+  LMOE_CK(h, cudaMemcpyAsync(h->xs[slot], x_host, x_bytes, cudaMemcpyHostToDevice, h->copy_in));
+  LMOE_CK(h, cudaEventRecord(h->ev_in[slot], h->copy_in));
+  // the forward on the caller's stream: after its x is in and after the
+  // output copy of two steps back has read this slot's y
+  LMOE_CK(h, cudaStreamWaitEvent(s, h->ev_in[slot], 0));
+  if (h->host_steps >= 2) LMOE_CK(h, cudaStreamWaitEvent(s, h->ev_out[slot], 0));
+  const int r = latentmoe_forward(h, h->xs[slot], h->ys[slot], T, st);
+  if (r != LATENTMOE_OK) return r;
+  LMOE_CK(h, cudaEventRecord(h->ev_fwd[slot], s));
+  // y out, behind the forward
+  LMOE_CK(h, cudaStreamWaitEvent(h->copy_out, h->ev_fwd[slot], 0));
+  LMOE_CK(h, cudaMemcpyAsync(out_host, h->ys[slot], y_bytes, cudaMemcpyDeviceToHost,
+                             h->copy_out));
+  LMOE_CK(h, cudaEventRecord(h->ev_out[slot], h->copy_out));
+  h->host_steps += 1;
+  return LATENTMOE_OK;
+}
+
+int latentmoe_host_wait(latentmoe_t h) {
+  if (h == nullptr) return LATENTMOE_ERR_INVALID_ARG;
+  LMOE_CK(h, cudaSetDevice(h->device));
+  if (h->copy_in) LMOE_CK(h, cudaStreamSynchronize(h->copy_in));
+  if (h->copy_out) LMOE_CK(h, cudaStreamSynchronize(h->copy_out));
   return LATENTMOE_OK;
 }
 

@@ -71,6 +71,9 @@ def test_null_arguments(lib):
     assert lib.latentmoe_create(ctypes.byref(d), 2, 0, None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_destroy(None) == capi.OK
     assert lib.latentmoe_forward(None, None, None, 1, None) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_forward_host(None, None, None, 1, None) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_forward_host_async(None, None, None, 1, None) == capi.ERR_INVALID_ARG
+    assert lib.latentmoe_host_wait(None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_load_weights(None, None, None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_get_status(None, None) == capi.ERR_INVALID_ARG
     assert lib.latentmoe_debug_gemm(None, None, None, 1, 128, 128, 0, None) == capi.ERR_INVALID_ARG

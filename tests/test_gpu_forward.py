@@ -114,6 +114,39 @@ def test_forward_host_matches_device_forward():
     assert torch.equal(yh, y_dev.cpu())
 
 
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_forward_host_async_pipeline_matches_device_forwards(out_fp32):
+    """Five pipelined host-buffer forwards of different inputs into different
+    outputs (the copies of one step overlapping the neighbours' forwards),
+    then one wait: each output equals the device forward of its input bit for
+    bit. Then the bench's pattern, one input and one output buffer reused for
+    three steps, and the synchronous entry afterwards."""
+    cfg = synth.LayerConfig("host-async", T=1500, d=512, l=256, E=8, k=2, F=512, Fs=256)
+    w = synth.make_weights(cfg, 17, "cuda")
+    layer = gh.make_layer(cfg, w, out_fp32=out_fp32)
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    xs = [synth.make_x(cfg, 100 + i, "cuda") for i in range(5)]
+    ys_dev = [layer.forward(x).clone() for x in xs]
+    torch.cuda.synchronize()
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.full((cfg.T, cfg.d), -1.0, dtype=dt).pin_memory() for _ in xs]
+    for a, b in zip(xh, yh):
+        layer.forward_host_async(a, b)
+    layer.host_wait()
+    for b, y in zip(yh, ys_dev):
+        assert torch.equal(b, y.cpu())
+    y1 = torch.full((cfg.T, cfg.d), -1.0, dtype=dt).pin_memory()
+    for _ in range(3):
+        layer.forward_host_async(xh[1], y1)
+    layer.host_wait()
+    assert torch.equal(y1, ys_dev[1].cpu())
+    y2 = torch.full((cfg.T, cfg.d), -1.0, dtype=dt).pin_memory()
+    layer.forward_host(xh[2], y2)
+    assert torch.equal(y2, ys_dev[2].cpu())
+    assert layer.status() == 0
+    layer.close()
+
+
 def test_launch_count_and_stage_times():
     cfg, w, x = _setup("tiny")
     layer = gh.make_layer(cfg, w)
