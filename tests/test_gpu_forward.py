@@ -351,3 +351,48 @@ def test_programmatic_launch_on_and_off_bitwise_equal(name):
     assert layer.status() == 0
     for y in ys[1:]:
         assert torch.equal(ys[0], y)
+
+
+@pytest.mark.parametrize("name,variant", [("tiny", "bf16"), ("mid", "bf16"),
+                                          ("imbalanced", "bf16"), ("mid", "one_sm"),
+                                          ("mid", "e4m3"), ("mid", "e4m3_dense")])
+def test_back_to_back_forwards_on_new_inputs(name, variant):
+    """Forwards enqueued back to back, each on new inputs (so each routes its
+    tokens differently), give the bits of the same forwards run one at a time
+    in plain stream order with a synchronisation between them. Under
+    programmatic launch each kernel's set-up overlaps the kernel before it,
+    across forwards too; every kernel must still read this forward's routing
+    and slots, never the previous forward's."""
+    cfg = synth.CONFIGS[name]
+    fp8 = variant.startswith("e4m3")
+    w = synth.make_weights(cfg, 11, "cuda")
+    xs = [synth.make_x(cfg, 20 + i, "cuda") for i in range(4)]
+    layer = gh.make_layer(cfg, w, fp8=fp8, fp8_dense=variant == "e4m3_dense")
+    if variant == "one_sm":
+        layer.set_sm_pairs(False)
+    scales = [0.02, 0.01, 0.02, 0.01, 0.02][:capi.FP8_TENSORS if variant == "e4m3_dense" else 2]
+
+    def run(pdl, sync):
+        layer.set_pdl(pdl)
+        if fp8:
+            layer.set_fp8_scales(scales)
+        ys = []
+        for x in xs:
+            ys.append(layer.forward(x).clone())
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        return ys
+
+    ys_fast = run(True, False)
+    ys_ref = run(False, True)
+    routes = set()
+    for i, (a, b) in enumerate(zip(ys_fast, ys_ref)):
+        assert torch.equal(a, b), f"forward {i}"
+    # the inputs do route differently (otherwise stale slots would go unseen)
+    for x in xs[:2]:
+        layer.forward(x)
+        routes.add(layer.get_routing(cfg.T, "cuda")["idx"].cpu().numpy().tobytes())
+    assert len(routes) == 2
+    layer.close()
