@@ -176,7 +176,7 @@ struct latentmoe {
   void* wmem = nullptr;          // one allocation holding every weight copy
   GemmMaps m_down, m_shared, m_up;  // dense GEMM maps (every box 128 rows)
   CUtensorMap m_wg, m_wu, m_wd;  // packed expert weights (grouped kernel)
-  CUtensorMap m_wr;              // router weights in router_bk(E)-column boxes (router kernel)
+  CUtensorMap m_wr;              // router weights in router_box_cols(E)-column boxes (router kernel)
   // workspace
   void* ws = nullptr;
   float* logits = nullptr;
@@ -794,7 +794,7 @@ int latentmoe_load_weights(latentmoe_t h, const latentmoe_weights* w,
   bool ok = true;
   ok &= make_map(&h->m_wr, o.w_r, E, dd, dd,
                  static_cast<uint32_t>(lmoe::router_w_box_rows(static_cast<int>(E))),
-                 static_cast<uint32_t>(lmoe::router_bk(static_cast<int>(E))));
+                 static_cast<uint32_t>(lmoe::router_box_cols(static_cast<int>(E))));
   if (h->fp8_dense)
     ok &= make_map_u8(&h->m_down.b, o.w_dn, l, dd, dd, 128);
   else
@@ -852,7 +852,7 @@ int forward_impl(latentmoe_t h, const void* x, void* out, int64_t T, cudaStream_
   CUtensorMap mx, mxr, mzp, mh, mc, msh;
   bool ok = make_map(&mx, x, T, dd, dd, 128);
   ok &= make_map(&mxr, x, T, dd, dd, 128,
-                 static_cast<uint32_t>(lmoe::router_bk(static_cast<int>(E))));
+                 static_cast<uint32_t>(lmoe::router_box_cols(static_cast<int>(E))));
   ok &= make_token_map(&mzp, h->zp, S, l, h->fp8);
   ok &= make_token_map(&mh, h->hb, S, F, h->fp8);
   CUtensorMap mx8;

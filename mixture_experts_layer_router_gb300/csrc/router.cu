@@ -30,6 +30,12 @@ static cudaError_t launch_router_impl(const CUtensorMap& x, const CUtensorMap& w
 
 cudaError_t launch_router_topk(const CUtensorMap& x, const CUtensorMap& w, RouterArgs a, int sms,
                                cudaStream_t s) {
+  if (router_bk(a.E) == 128) {
+    if (a.k <= 2) return launch_router_impl<2, 128>(x, w, a, sms, s);
+    if (a.k <= 4) return launch_router_impl<4, 128>(x, w, a, sms, s);
+    if (a.k <= 8) return launch_router_impl<8, 128>(x, w, a, sms, s);
+    return launch_router_impl<16, 128>(x, w, a, sms, s);
+  }
   if (router_bk(a.E) == 64) {
     if (a.k <= 2) return launch_router_impl<2, 64>(x, w, a, sms, s);
     if (a.k <= 4) return launch_router_impl<4, 64>(x, w, a, sms, s);

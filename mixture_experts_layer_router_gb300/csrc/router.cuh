@@ -36,12 +36,18 @@
 namespace lmoe {
 
 // k-blocks: 32 columns (64-byte swizzle) for E > 256, where a stage holds
-// 512 rows of W_r (40 KB; four stages fit), and 64 columns (128-byte swizzle)
-// for E <= 256: the TMA then reads 128-byte row pieces of x and W_r instead of
-// 64-byte ones, half the requests for the same bytes (at E = 64, 24 KB stages,
-// seven of them). The ring takes all the shared memory the exchange leaves.
-constexpr int kRBK = 32;
-__host__ __device__ constexpr int router_bk(int E) { return E <= 256 ? 64 : 32; }
+// 512 rows of W_r (40 KB; four stages fit); 64 columns (128-byte swizzle) for
+// E <= 256: the TMA then reads 128-byte row pieces of x and W_r instead of
+// 64-byte ones, half the requests for the same bytes; and for E <= 128, 128
+// columns as two 128-byte-swizzled atoms side by side, loaded by two TMA
+// copies issued back to back, so that each x row is read as 256 contiguous
+// bytes at a time (at E = 64, four 48 KB stages). The ring takes all the
+// shared memory the exchange leaves.
+__host__ __device__ constexpr int router_bk(int E) { return E <= 128 ? 128 : E <= 256 ? 64 : 32; }
+// Columns of one TMA box of x and W_r (one swizzle atom wide).
+__host__ __device__ constexpr int router_box_cols(int E) {
+  return router_bk(E) < 64 ? router_bk(E) : 64;
+}
 constexpr int kRMaxStages = 16;
 constexpr int kREpiWarps = 16;
 constexpr int kRThreads = 64 + 32 * kREpiWarps;  // producer, MMA, 16 epilogue warps
@@ -154,7 +160,8 @@ __device__ __forceinline__ void rank_merge(float (&sv)[K], int (&si)[K], const f
       if ((j & st) == 0) rank_cswap(sv[j], si[j], sv[j + st], si[j + st]);
 }
 
-// BK = router_bk(E): the k-block width the tensor maps were made with.
+// BK = router_bk(E): the k-block width; the tensor maps' boxes are
+// router_box_cols(E) columns wide (BK / 64 atoms per k-block for BK = 128).
 template <int KMAX, int BK>
 __global__ void __launch_bounds__(kRThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -163,8 +170,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int kATile = 128 * BK * 2;  // x
-  constexpr int kBBox = 256 * BK * 2;   // W_r per 256 experts
+  constexpr int kAtoms = BK > 64 ? BK / 64 : 1;
+  constexpr int kAtomCols = BK / kAtoms;
+  constexpr int kXAtom = 128 * kAtomCols * 2;
+  constexpr int kKPerAtom = kAtomCols / 16;
   const int stage_bytes = router_stage_bytes(a.E);
+  // W_r atom (box b, atom j at sb + (b * kAtoms + j) * w_atom)
+  const int w_atom = (a.E <= 256 ? router_w_box_rows(a.E) : 256) * kAtomCols * 2;
   RouterExchange<KMAX>* xch = reinterpret_cast<RouterExchange<KMAX>*>(smem);
   uint8_t* tiles = smem + ((sizeof(RouterExchange<KMAX>) + 1023) & ~static_cast<size_t>(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(tiles + a.stages * stage_bytes);
@@ -233,9 +245,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
           uint8_t* sa = tiles + stage * stage_bytes;
           uint8_t* sb = sa + kATile;
           mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          tma_load_2d(&tmX, &full_bar[stage], sa, kb * BK, t * 128, pol_x);
+#pragma unroll
+          for (int j = 0; j < kAtoms; ++j)
+            tma_load_2d(&tmX, &full_bar[stage], sa + j * kXAtom, kb * BK + j * kAtomCols, t * 128,
+                        pol_x);
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(&tmW, &full_bar[stage], sb + b * kBBox, kb * BK, b * 256, pol_w);
+#pragma unroll
+            for (int j = 0; j < kAtoms; ++j)
+              tma_load_2d(&tmW, &full_bar[stage], sb + (b * kAtoms + j) * w_atom,
+                          kb * BK + j * kAtomCols, b * 256, pol_w);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == a.stages) {
@@ -267,16 +285,21 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
           tc_fence_after_sync();
           const uint8_t* sa = tiles + stage * stage_bytes;
-          const uint64_t da = BK == 64 ? smem_desc_sw128(sa) : smem_desc_sw64(sa);
-          const uint64_t db0 =
-              BK == 64 ? smem_desc_sw128(sa + kATile) : smem_desc_sw64(sa + kATile);
-          const uint64_t db1 = BK == 64 ? smem_desc_sw128(sa + kATile + kBBox)
-                                        : smem_desc_sw64(sa + kATile + kBBox);
+          const uint8_t* sb = sa + kATile;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            tc_mma(tmem_base, da + 2ull * k, db0 + 2ull * k, id0, accum);
-            if (n1 > 0) tc_mma(tmem_base + 256, da + 2ull * k, db1 + 2ull * k, id1, accum);
+          for (int j = 0; j < kAtoms; ++j) {
+            const uint8_t* xa = sa + j * kXAtom;
+            const uint8_t* w0 = sb + j * w_atom;
+            const uint8_t* w1 = sb + (kAtoms + j) * w_atom;  // second 256 experts (E > 256)
+            const uint64_t da = kAtomCols == 64 ? smem_desc_sw128(xa) : smem_desc_sw64(xa);
+            const uint64_t db0 = kAtomCols == 64 ? smem_desc_sw128(w0) : smem_desc_sw64(w0);
+            const uint64_t db1 = kAtomCols == 64 ? smem_desc_sw128(w1) : smem_desc_sw64(w1);
+#pragma unroll
+            for (int k = 0; k < kKPerAtom; ++k) {
+              const uint32_t accum = (kb | j | k) != 0 ? 1u : 0u;
+              tc_mma(tmem_base, da + 2ull * k, db0 + 2ull * k, id0, accum);
+              if (n1 > 0) tc_mma(tmem_base + 256, da + 2ull * k, db1 + 2ull * k, id1, accum);
+            }
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == a.stages) {
@@ -297,6 +320,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     const int sub = (warp - 2) >> 2;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int nchunks = (a.E + 31) / 32;
+    const int ngroups = (a.E + 7) / 8;
     const int k = a.k;
     const int bar_id = 1 + quarter;
     uint32_t acc_phase = 0;
@@ -316,11 +340,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
         si[j] = 0x7fffffff;
       }
       float* lrow = a.logits + static_cast<long long>(row) * a.E;
-      for (int c = sub; c < nchunks; c += 4) {
+      {
 #pragma unroll 1
-        for (int g8 = 0; g8 < 4; ++g8) {
-          const int e0 = c * 32 + g8 * 8;
-          if (e0 >= a.E) break;
+        for (int g8 = sub; g8 < ngroups; g8 += 4) {
+          const int e0 = g8 * 8;
           uint32_t v[8];
           tmem_ld_8cols(lane_base + e0, v);
           tmem_ld_wait();
