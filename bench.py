@@ -526,14 +526,21 @@ def run_ours(args, cfg, rank, world, dist):
             layer.forward_host_async(xh, yh)
         layer.host_wait()
         n_e2e = max(3, min(args.steps, 20))
+        # its own clock record: this region runs at whatever clock the power
+        # cap allows by then, which can differ from the device-timed region's
+        e2e_clocks = ClockSampler(local)
+        e2e_clocks.start()
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
+        e2e_wall0 = time.time()
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             layer.forward_host_async(xh, yh)
         layer.host_wait()
+        e2e_wall1 = time.time()
         dt = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
+        e2e_clk = e2e_clocks.stop(e2e_wall0, e2e_wall1)
         if dist is not None:
             dist.barrier()
         t1 = time.perf_counter()
@@ -542,7 +549,7 @@ def run_ours(args, cfg, rank, world, dist):
         dt_sync = max_over_ranks(time.perf_counter() - t1, dist, "cuda")
         e2e = {"value": world * cfg.T * n_e2e / dt, "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
-               "steps": n_e2e,
+               "steps": n_e2e, "clocks": e2e_clk,
                "entry": "latentmoe_forward_host_async (copies overlap the neighbouring "
                         "steps' forwards), then latentmoe_host_wait",
                "synchronous": {"value": world * cfg.T * n_e2e / dt_sync, "unit": "tokens/s",
