@@ -9,8 +9,8 @@
 // One CTA owns 128 token rows and all E <= 512 experts: L = x W_r^T (+ b)
 // accumulates in TMEM (128 lanes x E columns, fp32) from TMA-fed tcgen05 MMAs
 // (M = 128 tokens, N = up to 256 experts per instruction). The x map reads
-// 128 rows x 32 columns per box, the W_r map router_w_box_rows(E) rows x 32
-// columns.
+// 128 rows x router_box_cols(E) columns per box, the W_r map
+// router_w_box_rows(E) rows x router_box_cols(E) columns.
 //
 // Epilogue: 16 warps, four per TMEM lane quarter (32 rows); the four warps
 // of a quarter split each row's experts.
