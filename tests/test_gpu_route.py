@@ -37,13 +37,20 @@ def _logits(T, E, seed, kind="normal"):
     (256, 8, 3, "zeros"), (16384, 512, 8, "normal"), (8192, 256, 7, "normal"), (1, 4, 1, "normal"),
     # around the one-CTA sort's limit (4096 slots): one CTA, then the cooperative launch
     (1024, 512, 4, "skewed"), (4097, 64, 1, "ties"),
+    # 2M slots: more 1024-slot chunks than the cooperative sort keeps resident
+    # on the SMs at once, so the three-launch sort runs
+    (262144, 32, 8, "normal"),
 ])
 def test_route_matches_oracle(T, E, k, kind):
     layer = _layer(E, k, T)
-    L = _logits(T, E, T * 31 + E, kind)
-    out = layer.route_from_logits(L.cuda())
+    L = _logits(T, E, T * 31 + E, kind).cuda()
+    n0 = layer.launch_count()
+    out = layer.route_from_logits(L)
     torch.cuda.synchronize()
-    ora = ref.route(L.double().numpy(), E, k)
+    if T * k > 1024 * 8 * torch.cuda.get_device_properties(0).multi_processor_count:
+        # top-k, then the sort's histogram, scan and scatter launches
+        assert layer.launch_count() - n0 == 4
+    ora = ref.route(L.cpu().double().numpy(), E, k)
     gh.assert_routing_equal(out, ora, T, k)
     assert layer.status() == 0
 
