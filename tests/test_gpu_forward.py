@@ -396,3 +396,19 @@ def test_back_to_back_forwards_on_new_inputs(name, variant):
         routes.add(layer.get_routing(cfg.T, "cuda")["idx"].cpu().numpy().tobytes())
     assert len(routes) == 2
     layer.close()
+
+
+@pytest.mark.parametrize("E,k", [(64, 4), (512, 8)])
+def test_router_several_tiles_per_cta(E, k):
+    """More 128-token tiles than SMs: each router CTA runs several tiles in
+    turn (its stage ring and TMEM hand-off carry over from tile to tile), at
+    both k-block widths (128 columns for E <= 128, 32 columns and two MMAs
+    for E = 512)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 128 * (2 * sms + 3) + 17  # every CTA two tiles or more, a ragged last tile
+    cfg = synth.LayerConfig("many-tiles", T=T, d=256, l=128, E=E, k=k, F=256)
+    w = synth.make_weights(cfg, 23, "cuda")
+    x = synth.make_x(cfg, 23, "cuda")
+    layer = gh.make_layer(cfg, w)
+    _check_layer(cfg, w, x, layer)
+    layer.close()
