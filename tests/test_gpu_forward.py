@@ -412,3 +412,37 @@ def test_router_several_tiles_per_cta(E, k):
     layer = gh.make_layer(cfg, w)
     _check_layer(cfg, w, x, layer)
     layer.close()
+
+
+def test_two_handles_on_two_streams():
+    """Two layers of different shapes, each on its own stream, forwards
+    interleaved with nothing ordering the streams: each output is bitwise the
+    one of the same forward run alone. The handles share no device state (each
+    has its own workspace, counters and scratch), so concurrency changes
+    nothing."""
+    cfg_a = synth.CONFIGS["mid"]
+    cfg_b = synth.LayerConfig("shared-b", T=1000, d=512, l=256, E=16, k=3, F=512, Fs=512)
+    wa = synth.make_weights(cfg_a, 31, "cuda")
+    wb = synth.make_weights(cfg_b, 32, "cuda")
+    xa = [synth.make_x(cfg_a, 40 + i, "cuda") for i in range(3)]
+    xb = [synth.make_x(cfg_b, 50 + i, "cuda") for i in range(3)]
+    la = gh.make_layer(cfg_a, wa)
+    lb = gh.make_layer(cfg_b, wb)
+    ref_a = [la.forward(x).clone() for x in xa]
+    ref_b = [lb.forward(x).clone() for x in xb]
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    ya = [torch.empty_like(y) for y in ref_a]
+    yb = [torch.empty_like(y) for y in ref_b]
+    for _ in range(2):
+        for i in range(3):
+            la.forward(xa[i], ya[i], stream=sa)
+            lb.forward(xb[i], yb[i], stream=sb)
+    torch.cuda.synchronize()
+    assert la.status() == 0 and lb.status() == 0
+    for a, b in zip(ya, ref_a):
+        assert torch.equal(a, b)
+    for a, b in zip(yb, ref_b):
+        assert torch.equal(a, b)
+    la.close()
+    lb.close()
